@@ -1,0 +1,221 @@
+"""Python face of the fp64 CPU oracle (``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the product library
+and its binding never do.  It shares no code with the CUDA path: it is built
+from ``oracle.c`` alone with the host C compiler.
+
+Every array the oracle sees is float64 (bf16 inputs are widened exactly by the
+caller) except the relayout, which copies opaque 16-bit words.
+
+What each function computes, and the page passage it follows, is stated in the
+header of ``oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "_oracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("sq", ctypes.c_int),
+        ("sk", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int),
+        ("q_offset", ctypes.c_int), ("key_len", ctypes.POINTER(ctypes.c_int32)),
+        ("scale", ctypes.c_double),
+    ]
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile an oracle source file with gcc (plain -O2, IEEE semantics kept)."""
+    tmp = out + ".tmp%d" % os.getpid()
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                           "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Build _oracle.so from oracle.c when it is missing or older than the source."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            compile_source(_SRC, _LIB)
+    return _LIB
+
+
+def open_library(path: str):
+    """Load a compiled oracle and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    pp = ctypes.POINTER(_Problem)
+    u16 = ctypes.POINTER(ctypes.c_uint16)
+    i = ctypes.c_int
+    lib.oracle_attn_fwd.argtypes = [pp, dp, dp, dp, dp, dp]
+    lib.oracle_attn_bwd.argtypes = [pp, dp, dp, dp, dp, dp, dp, dp]
+    lib.oracle_attn_fwd_rows.argtypes = [pp, dp, dp, dp, i, i, i, i, dp, dp]
+    lib.oracle_attn_bwd_rows.argtypes = [pp, dp, dp, dp, dp, i, i, i, i, dp, i, i, dp, dp]
+    lib.oracle_seq2head.argtypes = [u16, u16, i, i, i, i, i]
+    lib.oracle_head2seq.argtypes = [u16, u16, i, i, i, i, i]
+    lib.oracle_set_threads.argtypes = [i]
+    for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_attn_fwd_rows,
+              lib.oracle_attn_bwd_rows, lib.oracle_seq2head, lib.oracle_head2seq,
+              lib.oracle_set_threads, lib.oracle_get_threads):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _default
+    if _default is None:
+        path = build()
+        with _lock:
+            if _default is None:
+                _default = open_library(path)
+    return _default
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype.itemsize != 2:
+        raise TypeError("relayout copies 16-bit words")
+    return a.view(np.uint16)
+
+
+class Problem:
+    """Shapes and mask of one attention problem (q: [B][sq][H][d], k/v: [B][sk][H][d])."""
+
+    def __init__(self, B, H, sq, sk, d, causal, q_offset=0, key_len=None, scale=None):
+        self.B, self.H, self.sq, self.sk, self.d = int(B), int(H), int(sq), int(sk), int(d)
+        self.causal = bool(causal)
+        self.q_offset = int(q_offset)
+        self.key_len = None if key_len is None else np.ascontiguousarray(
+            np.asarray(key_len, dtype=np.int32))
+        self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+    @classmethod
+    def of(cls, q, k, causal, q_offset=0, key_len=None, scale=None) -> "Problem":
+        B, sq, H, d = q.shape
+        return cls(B, H, sq, k.shape[1], d, causal, q_offset, key_len, scale)
+
+    def c_struct(self) -> _Problem:
+        kl = (self.key_len.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+              if self.key_len is not None else ctypes.POINTER(ctypes.c_int32)())
+        return _Problem(self.B, self.H, self.sq, self.sk, self.d, int(self.causal),
+                        self.q_offset, kl, self.scale)
+
+
+class Oracle:
+    """Typed calls into one compiled oracle library (the default build, or a test's mutant)."""
+
+    def __init__(self, lib):
+        self.lib = lib
+
+    def set_threads(self, n: int) -> None:
+        """Thread count of the task pool (0 = all online cores)."""
+        self.lib.oracle_set_threads(int(n))
+
+    def threads(self) -> int:
+        return int(self.lib.oracle_get_threads())
+
+    def attn_fwd(self, q, k, v, causal, q_offset=0, key_len=None, scale=None):
+        """out [B][sq][H][d], lse [B][H][sq] (natural log) for all rows."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        out = np.empty_like(q)
+        lse = np.empty((P.B, P.H, P.sq), dtype=np.float64)
+        cp = P.c_struct()
+        if self.lib.oracle_attn_fwd(ctypes.byref(cp), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                    _ptr(lse)):
+            raise ValueError("oracle_attn_fwd rejected the problem")
+        return out, lse
+
+    def attn_bwd(self, q, k, v, dout, causal, q_offset=0, key_len=None, scale=None):
+        """dq [B][sq][H][d], dk/dv [B][sk][H][d] for all rows."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+        cp = P.c_struct()
+        if self.lib.oracle_attn_bwd(ctypes.byref(cp), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                    _ptr(dq), _ptr(dk), _ptr(dv)):
+            raise ValueError("oracle_attn_bwd rejected the problem")
+        return dq, dk, dv
+
+    def attn_fwd_rows(self, q, k, v, b, h, i0, i1, causal, q_offset=0, key_len=None,
+                      scale=None):
+        """out [i1-i0][d], lse [i1-i0] for query rows [i0, i1) of head (b, h)."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        out = np.empty((max(i1 - i0, 0) + 1, P.d), dtype=np.float64)
+        lse = np.empty((max(i1 - i0, 0) + 1,), dtype=np.float64)
+        cp = P.c_struct()
+        if self.lib.oracle_attn_fwd_rows(ctypes.byref(cp), _ptr(q), _ptr(k), _ptr(v), b, h,
+                                         i0, i1, _ptr(out), _ptr(lse)):
+            raise ValueError("oracle_attn_fwd_rows rejected the request")
+        return out[: i1 - i0], lse[: i1 - i0]
+
+    def attn_bwd_rows(self, q, k, v, dout, b, h, i0, i1, j0, j1, causal, q_offset=0,
+                      key_len=None, scale=None):
+        """dq rows [i0, i1) and dk/dv rows [j0, j1) of head (b, h)."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        dq = np.zeros((max(i1 - i0, 0) + 1, P.d), dtype=np.float64)
+        dk = np.zeros((max(j1 - j0, 0) + 1, P.d), dtype=np.float64)
+        dv = np.zeros((max(j1 - j0, 0) + 1, P.d), dtype=np.float64)
+        cp = P.c_struct()
+        if self.lib.oracle_attn_bwd_rows(ctypes.byref(cp), _ptr(q), _ptr(k), _ptr(v),
+                                         _ptr(dout), b, h, i0, i1, _ptr(dq), j0, j1,
+                                         _ptr(dk), _ptr(dv)):
+            raise ValueError("oracle_attn_bwd_rows rejected the request")
+        return dq[: i1 - i0], dk[: j1 - j0], dv[: j1 - j0]
+
+    def seq2head(self, x, N, b, s, h, d) -> np.ndarray:
+        """[N][b][s/N][h][d] -> [N][b][s][h/N][d], as opaque 16-bit words."""
+        x = _u16(x)
+        out = np.empty((N, b, s, h // N, d), dtype=np.uint16)
+        if self.lib.oracle_seq2head(x.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                    N, b, s, h, d):
+            raise ValueError("oracle_seq2head: s and h must divide by N")
+        return out
+
+    def head2seq(self, x, N, b, s, h, d) -> np.ndarray:
+        """[N][b][s][h/N][d] -> [N][b][s/N][h][d], as opaque 16-bit words."""
+        x = _u16(x)
+        out = np.empty((N, b, s // N, h, d), dtype=np.uint16)
+        if self.lib.oracle_head2seq(x.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                    N, b, s, h, d):
+            raise ValueError("oracle_head2seq: s and h must divide by N")
+        return out
+
+
+def default() -> Oracle:
+    """The oracle built from oracle.c in this directory."""
+    return Oracle(_load())
+
+
+def __getattr__(name):
+    # module-level shortcuts: oracle.attn_fwd(...), oracle.seq2head(...), ...
+    if name in ("set_threads", "threads", "attn_fwd", "attn_bwd", "attn_fwd_rows",
+                "attn_bwd_rows", "seq2head", "head2seq"):
+        return getattr(default(), name)
+    raise AttributeError(name)
