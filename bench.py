@@ -1,0 +1,440 @@
+"""Throughput of the Ulysses attention step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is the whole hot path over one batch of synthetic input, already
+resident in HBM:
+    seq->head relayout of Q/K/V, attention forward, head->seq relayout of O,
+    seq->head relayout of dO, attention backward (row statistics, main kernel,
+    dQ convert), head->seq relayout of dQ/dK/dV.
+The metric is causal attention fwd+bwd TFLOP/s (fwd = 4*b*h*s^2*d/2 flops for a
+causal square, backward 2.5x the forward), with the bf16 tensor-core fraction
+and the relayout GB/s against the measured HBM copy bandwidth beside it.
+
+N > 1 (one process per GPU under torch.distributed.run): every rank runs the
+same step on its own GPU with no collective on the data path (weak scaling);
+the timed region is bracketed by barriers and the slowest rank's time is used.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import contextlib
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+import torch.distributed as dist
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sequence_head_attention_seq_b300 import workloads  # noqa: E402
+
+METRIC = "causal MHA fwd+bwd TFLOP/s and % bf16 tensor peak; relayout GB/s vs HBM"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "llama70b"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+PROFILE_NOTES = os.path.join(ROOT, "profiles")
+
+
+# ---------------------------------------------------------------- accounting
+
+def attn_fwd_flops(w) -> float:
+    """4*b*h*sq*sk*d for the two GEMMs of the forward, halved for a causal square."""
+    f = 4.0 * w.b * w.h * w.s * w.s * w.d
+    return f / 2 if w.causal else f
+
+
+def step_flops(w) -> float:
+    return 3.5 * attn_fwd_flops(w)          # forward + backward (2.5x forward)
+
+
+def tensor_bytes(w) -> int:
+    return w.b * w.s * w.h * w.d * 2
+
+
+def relayout_bytes_per_step(w) -> int:
+    """Each relayout reads and writes every tensor once: Q, K, V, O, dO, dQ, dK, dV."""
+    return 0 if w.N == 1 else 8 * 2 * tensor_bytes(w)
+
+
+def launches_per_step(w) -> int:
+    relayouts = 0 if w.N == 1 else 4
+    return relayouts + 1 + 3              # fwd; bwd = statistics + main + dQ convert
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sequence_head_attention_seq_b300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_note: str, sources) -> int | None:
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    path = os.path.join(PROFILE_NOTES, kernel_note)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != source_digest(sources):
+        return None
+    return int(m.group(1))
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, device) -> float:
+    if dist.is_available() and dist.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def barrier():
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(REASON_NAMES, parts[3:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.out.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_index_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample(w, heads: int, prefix: int):
+    """Causal fwd+bwd of `heads` heads over the first `prefix` positions of workload w,
+    drawn with the workload's seeds and scale (a bounded sample of the same problem)."""
+    import oracle
+    orc = oracle.default()
+    shape = (1, prefix, heads, w.d)
+    q = workloads.randn_bf16(shape, w.seed("q"), w.scale).double().numpy()
+    k = workloads.randn_bf16(shape, w.seed("k"), w.scale).double().numpy()
+    v = workloads.randn_bf16(shape, w.seed("v"), w.scale).double().numpy()
+    do = workloads.randn_bf16(shape, w.seed("dout"), 1.0).double().numpy()
+    t0 = time.perf_counter()
+    orc.attn_fwd(q, k, v, w.causal)
+    orc.attn_bwd(q, k, v, do, w.causal)
+    dt = time.perf_counter() - t0
+    flops = 3.5 * 4.0 * heads * prefix * prefix * w.d / (2 if w.causal else 1)
+    return flops, dt, orc.threads()
+
+
+def cpu_baseline(w, heads=4, prefix=8192):
+    flops, dt, cores = oracle_sample(w, heads, prefix)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 C oracle, causal fwd+bwd of {heads} heads over the first {prefix} "
+                      f"positions of {w.name} (d={w.d}); {flops / 1e9:.1f} GFLOP in {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    heads, prefix = 1, 8192
+    for _ in range(args.warmup):
+        oracle_sample(w, heads, prefix)
+    total_flops, total_t, cores = 0.0, 0.0, 1
+    for _ in range(args.steps):
+        f, dt, cores = oracle_sample(w, heads, prefix)
+        total_flops += f
+        total_t += dt
+    value = total_flops / total_t / 1e12
+    sample = (f"fp64 C oracle, causal fwd+bwd of {heads} head over the first {prefix} positions "
+              f"of {w.name} per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "b": w.b, "heads": w.h, "head_dim": w.d, "seq_len": w.s,
+            "sp_degree": w.N, "heads_per_group": w.h_local, "causal": w.causal,
+            "input_scale": w.scale,
+            "l2": f"inputs larger than L2 ({tensor_bytes(w) / 2**20:.0f} MiB per tensor, 126 MB L2)",
+            "flops_convention": "fwd 4*b*h*s^2*d/2 (causal), bwd 2.5x fwd"}
+
+
+class EventTimer:
+    """CUDA events around each library call, recorded on the current (launching) stream."""
+
+    def __init__(self):
+        self.enabled = False
+        self.pairs = {}
+
+    @contextlib.contextmanager
+    def __call__(self, name):
+        if not self.enabled:
+            yield
+            return
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        yield
+        b.record()
+        self.pairs.setdefault(name, []).append((a, b))
+
+    def mean_ms(self):
+        return {n: sum(a.elapsed_time(b) for a, b in ps) / len(ps) for n, ps in self.pairs.items()}
+
+
+def run_ours(args, w):
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from sequence_head_attention_seq_b300 import UlyssesAttention, sp_get_device_status
+
+    peaks, peak_kind = load_peaks()
+    ins = workloads.make_inputs(w, device=device)
+    timer = EventTimer()
+    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=ins["key_len"],
+                            device=device, timer=timer)
+
+    def one_step():
+        step.forward(ins["q"], ins["k"], ins["v"])
+        step.backward(ins["dout"])
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    if sp_get_device_status() != 0:
+        raise RuntimeError("device status reported an error during warm-up")
+
+    clocks = ClockSampler(gpu_index_for(local))
+    clocks.start()
+    timer.enabled = True
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        one_step()
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    timer.enabled = False
+    clocks.stop()
+    local_ms = start.elapsed_time(end)
+    calls = timer.mean_ms()
+    status = sp_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    total_ms = reduce_max(local_ms, device)
+    ms_per_step = total_ms / args.steps
+    value = world * step_flops(w) * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host buffers in, results back out
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: ins[n].cpu().pin_memory() for n in ("q", "k", "v", "dout")}
+        host_out = [torch.empty(step.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(4)]
+        dev_in = {n: torch.empty_like(ins[n]) for n in host_in}
+
+        def e2e_step():
+            for n in host_in:
+                dev_in[n].copy_(host_in[n], non_blocking=True)
+            step.forward(dev_in["q"], dev_in["k"], dev_in["v"])
+            step.backward(dev_in["dout"])
+            for dst, src in zip(host_out, (step.o, step.dq, step.dk, step.dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        e2e_steps = max(1, min(args.steps, 5))
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = reduce_max(e0.elapsed_time(e1), device) / e2e_steps
+        e2e = {"value": world * step_flops(w) / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 4 * tensor_bytes(w), "d2h_bytes_per_step": 4 * tensor_bytes(w),
+               "ms_per_step": e2e_ms}
+
+    clock_summary = clocks.summary()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    fwd_ms = calls.get("attn_fwd")
+    bwd_ms = calls.get("attn_bwd")
+    fwd_f = attn_fwd_flops(w)
+    peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    bwd_tf = 2.5 * fwd_f / (bwd_ms * 1e-3) / 1e12
+    traffic = recorded_traffic("attn_bwd_llama70b.md", ["attn_bwd.cu", "ptx.cuh"])
+    relayout_ms = sum(calls.get(n, 0.0) for n in ("seq2head_qkv", "head2seq_o", "seq2head_do",
+                                                    "head2seq_grads"))
+    relayout = None
+    if relayout_ms > 0:
+        gbs = relayout_bytes_per_step(w) / (relayout_ms * 1e-3) / 1e9
+        relayout = {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "bytes_per_step": relayout_bytes_per_step(w), "ms_per_step": relayout_ms}
+    kernels = {}
+    for n, ms in calls.items():
+        entry = {"ms": ms}
+        if n == "attn_fwd":
+            entry["tflops"] = fwd_f / (ms * 1e-3) / 1e12
+        elif n == "attn_bwd":
+            entry["tflops"] = 2.5 * fwd_f / (ms * 1e-3) / 1e12
+        else:
+            tensors = 3 if n in ("seq2head_qkv", "head2seq_grads") else 1
+            entry["gbs"] = tensors * 2 * tensor_bytes(w) / (ms * 1e-3) / 1e9
+        kernels[n] = entry
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)*scale bf16, shapes of the workload)",
+        "config": config_of(w),
+        "pct_bf16_peak": {"burst": value / peak_burst, "sustained": value / peak_sus,
+                          "peaks": peak_kind},
+        "roofline": {"kernel": "sp_attn_bwd (statistics + tcgen05 main + dQ convert)",
+                     "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": bwd_tf / peak_sus, "peak_kind": f"{peak_kind} sustained bf16",
+                     "frac_of_burst": bwd_tf / peak_burst, "traffic": traffic,
+                     "algorithmic_flops_per_launch": 2.5 * fwd_f},
+        "relayout": relayout,
+        "kernels": kernels,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(w) * args.steps,
+        "clocks": clock_summary,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+/*
+ * sp.h -- C ABI of libsp: causal multi-head attention on the Ulysses
+ * sequence/head layout, forward and backward, for NVIDIA B300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are bf16 in DEVICE memory, owned by the caller; the library never
+ *    allocates, frees or keeps a pointer after a call returns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
+ *    enqueues work on it: no host synchronisation, no allocation.
+ *  - Argument errors are detected on the host and returned BEFORE anything is
+ *    launched (SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_MISALIGNED).
+ *  - A failed launch returns SP_ERR_CUDA.  Faults found while the kernels run
+ *    (a device wait that gave up) are reported by sp_get_device_status().
+ *  - Calls are thread-safe; the library holds no per-call state.
+ */
+#ifndef SP_H
+#define SP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sp_status {
+    SP_OK = 0,
+    SP_ERR_INVALID_ARG = 1,  /* a size, count, flag or pointer is out of range */
+    SP_ERR_UNSUPPORTED = 2,  /* valid in principle, not implemented (e.g. head_dim not 64/128) */
+    SP_ERR_MISALIGNED = 3,   /* a pointer or stride breaks the 16-byte rule */
+    SP_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    SP_ERR_TIMEOUT = 5,      /* a device-side wait exceeded its limit; results are invalid */
+    SP_ERR_WORKSPACE = 6     /* the workspace passed to sp_attn_bwd is too small */
+} sp_status;
+
+#define SP_MAX_RELAYOUT_TENSORS 8
+
+/*
+ * Ulysses regrouping: sequence shards -> head groups.
+ *
+ * Defined by: long-context-attention issue "关于数据分割和合并" (each rank
+ * starts with 1/N of the sequence of Q/K/V, an all-to-all that works like a
+ * transpose gives every rank the full sequence for a subset of the heads);
+ * transformers PR 31525 "Support deepspeed sequence parallel" (shard r holds
+ * rows [r*s/N, (r+1)*s/N), inputs of the all-to-all are [b, s/p, n, h]);
+ * "Parallel multi-head attention", section 2.2 (heads are assigned to devices
+ * in contiguous blocks).  On one GPU the all-to-all is this local permutation.
+ *
+ *   in[t]  : [N][b][s/N][h][d]   shard r = sequence rows r*s/N .. (r+1)*s/N-1
+ *   out[t] : [N][b][s][h/N][d]   group g = heads g*h/N .. (g+1)*h/N-1
+ *   out[t][g][bb][r*s/N+u][j][c] = in[t][r][bb][u][g*h/N+j][c]
+ *
+ * in, out : HOST arrays of `ntensors` DEVICE pointers (1 <= ntensors <= 8), so
+ *           Q, K and V (or dQ, dK, dV) move in one launch.  Elements are copied
+ *           as opaque 16-bit words: the result is bit-exact.  in[t] and out[t]
+ *           must not overlap.  Pointers 16-byte aligned.
+ * Errors  : N < 1, b/s/h/d < 1, s % N or h % N != 0 -> SP_ERR_INVALID_ARG;
+ *           a NULL pointer -> SP_ERR_INVALID_ARG; misalignment -> SP_ERR_MISALIGNED.
+ */
+sp_status sp_relayout_seq2head(const void* const* in, void* const* out, int ntensors,
+                               int N, int b, int s, int h, int d, void* stream);
+
+/*
+ * Inverse regrouping: head groups -> sequence shards (the all-to-all after
+ * attention in the same pages; each rank's output is (b, s/N, hidden)).
+ *
+ *   in[t]  : [N][b][s][h/N][d],  out[t] : [N][b][s/N][h][d]
+ * Arguments and errors as sp_relayout_seq2head.
+ */
+sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int ntensors,
+                               int N, int b, int s, int h, int d, void* stream);
+
+/*
+ * One attention problem.  Sources: "adv07: Sequence Parallel" (mini-vllm
+ * tutorial), section 3 Q4: out[i] = softmax(q[i] K^T / sqrt(d)) V with a causal
+ * mask that hides only future keys (j > i), a query shard masking by its GLOBAL
+ * row position; section 4: a query shard attends to the full K/V prefix.
+ * "Parallel multi-head attention", section 3.2: scores / sqrt(head_dim), an
+ * additive mask, softmax in fp32.  transformers PR 31525: a key-padding mask
+ * from (input_ids != pad).
+ *
+ * Key j is visible from query row i of batch entry bb iff
+ *     (!causal || j <= q_offset + i)  &&  (key_len == NULL || j < key_len[bb]).
+ * A row with no visible key returns out = 0, lse = -inf and no gradient.
+ *
+ * Layout: q, o, dout, dq are [B][sq][H][d]; k, v, dk, dv are [B][sk][H][d];
+ * d is contiguous and the other strides (in ELEMENTS) are given per tensor.
+ * Strides must be multiples of 8 elements and pointers 16-byte aligned.
+ */
+typedef struct sp_attn_params {
+    const void* q;            /* bf16, device */
+    const void* k;            /* bf16, device */
+    const void* v;            /* bf16, device */
+    int64_t q_stride[3];      /* batch, seq, head strides of q and dq */
+    int64_t k_stride[3];      /* ... of k and dk */
+    int64_t v_stride[3];      /* ... of v and dv */
+    int64_t o_stride[3];      /* ... of o and dout */
+    int B, H;                 /* batch entries (e.g. N*b head groups) and heads per entry */
+    int sq, sk;               /* query rows and key rows */
+    int d;                    /* head_dim: 64 or 128 */
+    int causal;               /* 0 or 1 */
+    int q_offset;             /* global sequence position of query row 0 (>= 0) */
+    const int32_t* key_len;   /* NULL, or DEVICE [B] valid-key counts in [0, sk] */
+    float softmax_scale;      /* <= 0 selects 1/sqrt(d) */
+} sp_attn_params;
+
+/*
+ * Forward: o = softmax(scale * q k^T + mask) v per (batch entry, head), and
+ * lse = log(sum_j exp(scale * q.k_j)) over the visible keys (natural log),
+ * both from fp32 accumulation; o is rounded to bf16 (nearest even).
+ *
+ * o   : DEVICE bf16, layout of q with o_stride.
+ * lse : DEVICE fp32 [B][H][sq], contiguous.  Needed by sp_attn_bwd.
+ * Errors: B, H, sq, sk < 0 or any of them 0 with others nonzero is allowed
+ *         (nothing to do -> SP_OK); causal with q_offset + sq > sk, q_offset < 0,
+ *         NULL pointers -> SP_ERR_INVALID_ARG; d not 64/128 -> SP_ERR_UNSUPPORTED;
+ *         pointer/stride alignment -> SP_ERR_MISALIGNED.
+ */
+sp_status sp_attn_fwd(const sp_attn_params* p, void* o, float* lse, void* stream);
+
+/*
+ * Bytes of device workspace sp_attn_bwd needs for `p` (fp32 dQ accumulator and
+ * per-row statistics, rounded up to 128-row tiles).  0 on invalid arguments.
+ */
+size_t sp_attn_bwd_workspace_size(const sp_attn_params* p);
+
+/*
+ * Backward of sp_attn_fwd given dout (no formulas on the pages; the textbook
+ * derivative of the forward definition, recomputing P from the saved lse):
+ *     D_i   = sum_c dout_ic o_ic
+ *     dS_ij = P_ij (dout_i . v_j - D_i)
+ *     dq_i  = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dout_i
+ * dq, dk, dv are written (not accumulated) in bf16 with the strides of q, k, v.
+ *
+ * o, lse     : the forward's outputs for the same p.
+ * workspace  : DEVICE, >= sp_attn_bwd_workspace_size(p) bytes, 256-byte aligned,
+ *              owned by the caller; its contents on entry do not matter.
+ * Errors as sp_attn_fwd, plus SP_ERR_WORKSPACE when workspace_bytes is too small.
+ */
+sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that the
+ * kernels set when a bounded device-side wait gives up (SP_ERR_TIMEOUT) or a
+ * launch-time invariant fails inside a kernel.  SP_ERR_CUDA if the stream
+ * reports an error.
+ */
+sp_status sp_get_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* sp_status_string(sp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SP_H */

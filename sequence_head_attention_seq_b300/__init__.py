@@ -1,1 +1,21 @@
-"""Causal multi-head attention on the Ulysses sequence/head layout, for B300 (sm_103a)."""
+"""Causal multi-head attention on the Ulysses sequence/head layout, for B300 (sm_103a).
+
+The computation lives in ``libsp.so`` (C ABI in ``include/sp.h``, CUDA kernels in
+``csrc/``).  This package is its thin binding:
+
+    sp_relayout_seq2head / sp_relayout_head2seq   sequence shards <-> head groups
+    sp_attn_fwd                                   attention forward (out + lse)
+    sp_attn_bwd                                   attention backward (dq, dk, dv)
+    UlyssesAttention                              the whole step on shard tensors
+
+Nothing here computes attention in Python; if the native library is missing the
+calls raise.
+"""
+from .binding import (SpError, sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd,
+                      sp_get_device_status, sp_relayout_head2seq, sp_relayout_seq2head,
+                      sp_status_string)
+from .pipeline import UlyssesAttention
+
+__all__ = ["SpError", "sp_attn_bwd", "sp_attn_bwd_workspace_size", "sp_attn_fwd",
+           "sp_get_device_status", "sp_relayout_head2seq", "sp_relayout_seq2head",
+           "sp_status_string", "UlyssesAttention"]

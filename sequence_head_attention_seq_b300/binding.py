@@ -1,0 +1,263 @@
+"""Thin ctypes binding of libsp (include/sp.h), same names as the C ABI.
+
+Only argument marshalling happens here: tensor checks, strides, data
+pointers and the current CUDA stream.  Every step of the computation runs in
+libsp's kernels.  PyTorch provides device memory and streams.
+
+If libsp.so cannot be loaded (or built), every call raises ``SpError``: there
+is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+SP_OK = 0
+STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED",
+                3: "SP_ERR_MISALIGNED", 4: "SP_ERR_CUDA", 5: "SP_ERR_TIMEOUT",
+                6: "SP_ERR_WORKSPACE"}
+MAX_RELAYOUT_TENSORS = 8
+
+# Every symbol include/sp.h declares.
+EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_attn_fwd",
+           "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_get_device_status",
+           "sp_status_string"]
+
+
+class SpError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = int(code)
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)}")
+
+
+class SpAttnParams(ctypes.Structure):
+    """Mirror of sp_attn_params."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("sq", ctypes.c_int), ("sk", ctypes.c_int),
+        ("d", ctypes.c_int), ("causal", ctypes.c_int), ("q_offset", ctypes.c_int),
+        ("key_len", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
+    ]
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libsp.so")
+
+
+def load(build_if_missing: bool = True):
+    """Load libsp.so (building it with nvcc first when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import build as _build
+        try:
+            if build_if_missing and _build.stale():
+                _build.build()
+        except Exception as e:  # noqa: BLE001 - report why the native library is unavailable
+            raise RuntimeError(f"libsp could not be built: {e}") from e
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libsp.so not found at {path}")
+        lib = ctypes.CDLL(path)
+        vpp = ctypes.POINTER(ctypes.c_void_p)
+        i = ctypes.c_int
+        for name in ("sp_relayout_seq2head", "sp_relayout_head2seq"):
+            f = getattr(lib, name)
+            f.argtypes = [vpp, vpp, i, i, i, i, i, i, ctypes.c_void_p]
+            f.restype = i
+        pp = ctypes.POINTER(SpAttnParams)
+        lib.sp_attn_fwd.argtypes = [pp, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        lib.sp_attn_fwd.restype = i
+        lib.sp_attn_bwd_workspace_size.argtypes = [pp]
+        lib.sp_attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.sp_attn_bwd.argtypes = [pp] + [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p]
+        lib.sp_attn_bwd.restype = i
+        lib.sp_get_device_status.argtypes = [ctypes.c_void_p]
+        lib.sp_get_device_status.restype = i
+        lib.sp_status_string.argtypes = [i]
+        lib.sp_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != SP_OK:
+        raise SpError(fn, rc)
+
+
+def _need_bf16_cuda(name: str, t: torch.Tensor) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _ptr_array(ts):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def _relayout(fn_name: str, inputs, N: int, b: int, s: int, h: int, d: int, out_shape, outs):
+    lib = load()
+    if not 1 <= len(inputs) <= MAX_RELAYOUT_TENSORS:
+        raise ValueError("relayout moves 1..8 tensors per call")
+    for n, t in enumerate(inputs):
+        _need_bf16_cuda(f"in[{n}]", t)
+        if not t.is_contiguous():
+            raise ValueError("relayout inputs must be contiguous")
+    if outs is None:
+        outs = [torch.empty(out_shape, dtype=torch.bfloat16, device=inputs[0].device)
+                for _ in inputs]
+    for n, t in enumerate(outs):
+        _need_bf16_cuda(f"out[{n}]", t)
+        if not t.is_contiguous() or t.numel() != math.prod(out_shape):
+            raise ValueError("relayout outputs must be contiguous with the output size")
+    pin, keep_in = _ptr_array(inputs)
+    pout, keep_out = _ptr_array(outs)
+    rc = getattr(lib, fn_name)(pin, pout, len(inputs), N, b, s, h, d, _stream(inputs[0].device))
+    _check(fn_name, rc)
+    return outs
+
+
+def sp_relayout_seq2head(inputs, N: int, outs=None):
+    """Sequence shards [N][b][s/N][h][d] -> head groups [N][b][s][h/N][d] (one launch)."""
+    x = inputs[0]
+    if x.dim() != 5 or x.shape[0] != N:
+        raise ValueError("expected [N][b][s/N][h][d] shard tensors")
+    _, b, sl, h, d = x.shape
+    if h % N:
+        raise ValueError("h must be divisible by N")
+    return _relayout("sp_relayout_seq2head", inputs, N, b, sl * N, h, d,
+                     (N, b, sl * N, h // N, d), outs)
+
+
+def sp_relayout_head2seq(inputs, N: int, outs=None):
+    """Head groups [N][b][s][h/N][d] -> sequence shards [N][b][s/N][h][d] (one launch)."""
+    x = inputs[0]
+    if x.dim() != 5 or x.shape[0] != N:
+        raise ValueError("expected [N][b][s][h/N][d] group tensors")
+    _, b, s, hl, d = x.shape
+    if s % N:
+        raise ValueError("s must be divisible by N")
+    return _relayout("sp_relayout_head2seq", inputs, N, b, s, hl * N, d,
+                     (N, b, s // N, hl * N, d), outs)
+
+
+def _same_layout(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """Equal strides on every dimension longer than 1 (others are never stepped)."""
+    return all(n == 1 or sa == sb for n, sa, sb in zip(a.shape, a.stride(), b.stride()))
+
+
+def _strides(t: torch.Tensor, name: str):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B][S][H][d]")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name}: head_dim must be contiguous")
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
+def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
+                softmax_scale=None) -> SpAttnParams:
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_bf16_cuda(name, t)
+    B, sq, H, d = q.shape
+    if k.shape[0] != B or k.shape[2] != H or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k and v must be [B][sk][H][d] matching q")
+    p = SpAttnParams()
+    p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    p.q_stride = _strides(q, "q")
+    p.k_stride = _strides(k, "k")
+    p.v_stride = _strides(v, "v")
+    p.o_stride = _strides(o_like, "o")
+    p.B, p.H, p.sq, p.sk, p.d = B, H, sq, k.shape[1], d
+    p.causal = 1 if causal else 0
+    p.q_offset = int(q_offset)
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
+            raise ValueError("key_len must be a CUDA int32 tensor of B entries")
+        p.key_len = key_len.data_ptr()
+    else:
+        p.key_len = None
+    p.softmax_scale = float(softmax_scale) if softmax_scale is not None else 0.0
+    return p
+
+
+def sp_attn_fwd(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
+                softmax_scale=None, out=None, lse=None):
+    """out [B][sq][H][d] bf16 and lse [B][H][sq] fp32 (natural log)."""
+    lib = load()
+    B, sq, H, d = q.shape
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if lse is None:
+        lse = torch.empty((B, H, sq), dtype=torch.float32, device=q.device)
+    _need_bf16_cuda("out", out)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, sq):
+        raise ValueError("lse must be contiguous fp32 [B][H][sq]")
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale)
+    rc = lib.sp_attn_fwd(ctypes.byref(p), out.data_ptr(), lse.data_ptr(), _stream(q.device))
+    _check("sp_attn_fwd", rc)
+    return out, lse
+
+
+def sp_attn_bwd_workspace_size(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
+                               softmax_scale=None) -> int:
+    lib = load()
+    p = make_params(q, k, v, q, causal, q_offset, key_len, softmax_scale)
+    return int(lib.sp_attn_bwd_workspace_size(ctypes.byref(p)))
+
+
+def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0, key_len=None,
+                softmax_scale=None, dq=None, dk=None, dv=None, workspace=None):
+    """dq, dk, dv (bf16, layouts of q, k, v) from the forward's out/lse and dout."""
+    lib = load()
+    _need_bf16_cuda("out", out)
+    _need_bf16_cuda("dout", dout)
+    if out.shape != dout.shape or not _same_layout(out, dout):
+        raise ValueError("out and dout must share shape and strides")
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale)
+    def like(t):
+        return torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=t.device)
+
+    dq = like(q) if dq is None else dq
+    dk = like(k) if dk is None else dk
+    dv = like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _need_bf16_cuda(name, t)
+        if t.shape != ref.shape or not _same_layout(t, ref):
+            raise ValueError(f"{name} must have the shape and strides of its input")
+    need = int(lib.sp_attn_bwd_workspace_size(ctypes.byref(p)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.sp_attn_bwd(ctypes.byref(p), out.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), _stream(q.device))
+    _check("sp_attn_bwd", rc)
+    return dq, dk, dv
+
+
+def sp_get_device_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the kernels' status code."""
+    lib = load()
+    return int(lib.sp_get_device_status(_stream(device)))
+
+
+def sp_status_string(code: int) -> str:
+    return load().sp_status_string(int(code)).decode()

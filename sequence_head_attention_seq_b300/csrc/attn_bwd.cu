@@ -1,0 +1,502 @@
+// attn_bwd.cu -- backward of the attention forward, on tcgen05.
+//
+// The pages give no backward formulas; this is the textbook derivative of
+// out_i = sum_j P_ij v_j with P_ij = exp(scale q_i.k_j - lse_i) over visible keys:
+//     D_i   = sum_c dout_ic out_ic
+//     dP_ij = dout_i . v_j,   dS_ij = P_ij (dP_ij - D_i)
+//     dq_i  = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dout_i
+//
+// Three launches:
+//   1. bwd_prep: per query row D_i and lse_i*log2(e) into the workspace (padded
+//      rows get lse = +inf, D = 0 so they contribute nothing), and zero the fp32
+//      dQ accumulator.  Bandwidth bound.
+//   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
+//      128-row query tiles that can see it (causal: from the diagonal down):
+//        warp 0      TMA producer (K, V once; Q_i, dO_i and row stats per tile, 2 stages)
+//        warp 1      MMA issuer and TMEM owner
+//        warps 4..7  P/dS computation (thread = one key row = one TMEM lane),
+//                    dQ drain, dK/dV epilogue
+//      TMEM (512 columns): [0,128) S^T then P^T (bf16, first half) and one dQ half,
+//      [128,256) dP^T then dS^T (bf16, first half) and the other dQ half,
+//      then dK and dV accumulators.
+//        S^T = K Q_i^T, dP^T = V dO_i^T        (A, B from shared memory, K-major)
+//        dV += P^T dO_i,  dK += dS^T Q_i       (A from TMEM, B MN-major in smem)
+//        dQ_i = dS K                           (dS written to smem by the P/dS
+//                                               warps, MN-major A; K MN-major B)
+//      dQ_i is added into the fp32 workspace with vector reductions.
+//   3. bwd_dq_convert: dq = bf16(scale * accumulator).  Bandwidth bound.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sp {
+namespace {
+
+constexpr int kRows = 128;   // query rows per tile
+constexpr int kKeys = 128;   // keys per CTA
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- 1. row statistics
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       int64_t os0, int64_t os1, int64_t os2,
+                                                       const float* __restrict__ lse,
+                                                       float* __restrict__ stats,
+                                                       float* __restrict__ dq_acc, int B, int H,
+                                                       int sq, int64_t rows) {
+  // one warp per (batch entry, head, padded row)
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  const int64_t total = static_cast<int64_t>(B) * H * rows;
+  if (wid >= total) return;
+  const int64_t i = wid % rows;
+  const int64_t bh = wid / rows;
+  const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+  constexpr int kPer = D / 32;   // elements per lane
+  float acc = 0.0f;
+  if (i < sq) {
+    const int64_t off = b * os0 + i * os1 + h * os2 + lane * kPer;
+    if constexpr (kPer == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+      const uint2 c = *reinterpret_cast<const uint2*>(dout + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float2 x = __bfloat1622float2(a2[k]);
+        const float2 y = __bfloat1622float2(c2[k]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    } else {
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + off);
+      const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(dout + off);
+      const float2 x = __bfloat1622float2(a);
+      const float2 y = __bfloat1622float2(c);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  float* srow = stats + bh * 2 * rows;
+  if (lane == 0) {
+    float l2 = INFINITY;   // padded or empty row: P = exp2(x - inf) = 0
+    if (i < sq) {
+      const float v = lse[bh * sq + i];
+      if (v != -INFINITY) l2 = v * kLog2e;
+    }
+    srow[i] = l2;
+    srow[rows + i] = (i < sq) ? acc : 0.0f;
+  }
+  float4* z = reinterpret_cast<float4*>(dq_acc + (bh * rows + i) * D);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = lane; c < D / 4; c += 32) z[c] = zero;
+}
+
+// ---------------------------------------------------------------- 3. dQ convert
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dq_acc,
+                                                             __nv_bfloat16* __restrict__ dq,
+                                                             int64_t qs0, int64_t qs1,
+                                                             int64_t qs2, int B, int H, int sq,
+                                                             int64_t rows, float scale) {
+  // thread = 8 consecutive elements of one row
+  constexpr int kVec = D / 8;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = static_cast<int64_t>(B) * H * sq * kVec;
+  if (t >= total) return;
+  const int c = static_cast<int>(t % kVec);
+  const int64_t row = t / kVec;   // (b, h, i) with i fastest
+  const int64_t i = row % sq;
+  const int64_t bh = row / sq;
+  const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + (bh * rows + i) * D + c * 8);
+  const float4 x = src[0], y = src[1];
+  uint4 out;
+  out.x = pack_bf16x2(x.x * scale, x.y * scale);
+  out.y = pack_bf16x2(x.z * scale, x.w * scale);
+  out.z = pack_bf16x2(y.x * scale, y.y * scale);
+  out.w = pack_bf16x2(y.z * scale, y.w * scale);
+  *reinterpret_cast<uint4*>(dq + b * qs0 + i * qs1 + h * qs2 + c * 8) = out;
+}
+
+// ---------------------------------------------------------------- 2. main kernel
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kTileBytes = kRows * D * 2;
+  alignas(1024) uint8_t k[kTileBytes];
+  alignas(1024) uint8_t v[kTileBytes];
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t dout[2][kTileBytes];
+  alignas(1024) uint8_t ds[kKeys * kRows * 2];    // dS as [key][query], 2 chunks of 64 queries
+  alignas(16) float stats[2][2][kRows];            // [stage][lse2 | D][row]
+  uint64_t kv_full, q_full[2], q_empty[2], s_full, p_full, dq_full, dq_empty, dkv_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct BwdKernelParams {
+  CUtensorMap tq, tk, tv, tdo;
+  const float* stats;     // [B][H][2][rows]
+  float* dq_acc;          // [B][H][rows][D]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int64_t k_stride[3], v_stride[3];
+  AttnGeom g;
+  int64_t rows;
+  int num_kv_tiles;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
+  int n = g.sk;
+  if (g.key_len != nullptr) n = min(n, max(__ldg(g.key_len + b), 0));
+  return n;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdKernelParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+  constexpr int kChunks = D / 64;
+  constexpr uint32_t kTileBytes = BwdSmem<D>::kTileBytes;
+  constexpr uint32_t kColS = 0, kColDP = 128;
+  constexpr uint32_t kColDK = 256, kColDV = 256 + D;
+
+  const AttnGeom& g = p.g;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.x % (g.B * g.H);
+  const int n = blockIdx.x / (g.B * g.H);          // key tile; small n = most work (causal)
+  const int b = bh / g.H, h = bh % g.H;
+  const int kv0 = n * kKeys;
+  const int kvlen = kv_limit(g, b);
+  const int m_start = g.causal ? max(0, kv0 - g.q_offset) / kRows : 0;
+  const int m_end = (g.sq + kRows - 1) / kRows;
+  const int nq = (kv0 < kvlen) ? max(0, m_end - m_start) : 0;
+
+  if (threadIdx.x == 0) {
+    if ((smem_u32(smem_raw) & 1023u) != 0) raise_status(p.status, kStatusBadSmem);
+    mbar_init(&sm.kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, kKeys);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_empty, kKeys);
+    mbar_init(&sm.dkv_full, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == 0 && lane == 0 && nq > 0) {
+    // ------------------------------------------------------------ TMA producer
+    tma_prefetch_desc(&p.tq);
+    tma_prefetch_desc(&p.tk);
+    tma_prefetch_desc(&p.tv);
+    tma_prefetch_desc(&p.tdo);
+    mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
+    for (int c = 0; c < kChunks; ++c) {
+      tma_load_4d(sm.k + c * 16384, &p.tk, &sm.kv_full, c * 64, h, kv0, b);
+      tma_load_4d(sm.v + c * 16384, &p.tv, &sm.kv_full, c * 64, h, kv0, b);
+    }
+    const float* st_base = p.stats + static_cast<int64_t>(bh) * 2 * p.rows;
+    for (int it = 0; it < nq; ++it) {
+      const int s = it & 1;
+      const int q0 = (m_start + it) * kRows;
+      if (it >= 2 && !mbar_wait(&sm.q_empty[s], ((it >> 1) - 1) & 1, p.status, abort_flag)) break;
+      mbar_expect_tx(&sm.q_full[s], 2 * kTileBytes + 2 * kRows * 4);
+      for (int c = 0; c < kChunks; ++c) {
+        tma_load_4d(sm.q[s] + c * 16384, &p.tq, &sm.q_full[s], c * 64, h, q0, b);
+        tma_load_4d(sm.dout[s] + c * 16384, &p.tdo, &sm.q_full[s], c * 64, h, q0, b);
+      }
+      bulk_load(sm.stats[s][0], st_base + q0, kRows * 4, &sm.q_full[s]);
+      bulk_load(sm.stats[s][1], st_base + p.rows + q0, kRows * 4, &sm.q_full[s]);
+    }
+  } else if (warp == 1 && lane == 0 && nq > 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16(kKeys, kRows, false, false);   // M = keys, N = queries
+    constexpr uint32_t kIdKV = idesc_bf16(kKeys, D, false, true);       // dK, dV: N = d
+    constexpr uint32_t kIdQ = idesc_bf16(kRows, 64, true, true);        // dQ half: N = 64
+    const uint32_t k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v), ds_addr = smem_u32(sm.ds);
+    bool ok = mbar_wait(&sm.kv_full, 0, p.status, abort_flag);
+    for (int it = 0; it < nq && ok; ++it) {
+      const int s = it & 1;
+      if (!(ok = mbar_wait(&sm.q_full[s], (it >> 1) & 1, p.status, abort_flag))) break;
+      if (it > 0 && !(ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(sm.q[s]), do_addr = smem_u32(sm.dout[s]);
+      // S^T = K Q^T and dP^T = V dO^T, contracting over d
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+        mma_ss(tmem + kColS, sdesc_sw128(k_addr + off, 16, 1024),
+               sdesc_sw128(q_addr + off, 16, 1024), kIdS, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+        mma_ss(tmem + kColDP, sdesc_sw128(v_addr + off, 16, 1024),
+               sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0);
+      }
+      mma_commit(&sm.s_full);
+      if (!(ok = mbar_wait(&sm.p_full, it & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      // dV += P^T dO, dK += dS^T Q, contracting over the 128 query rows
+#pragma unroll
+      for (int kk = 0; kk < kRows / 16; ++kk) {
+        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+        mma_ts(tmem + kColDV, tmem + kColS + kk * 8,
+               sdesc_sw128(do_addr + kk * 2048, 16384, 1024), kIdKV, acc);
+        mma_ts(tmem + kColDK, tmem + kColDP + kk * 8,
+               sdesc_sw128(q_addr + kk * 2048, 16384, 1024), kIdKV, acc);
+      }
+      // dQ = dS K, contracting over the 128 keys; N = d split in halves of 64
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk) {
+#pragma unroll
+        for (int hf = 0; hf < kChunks; ++hf)
+          mma_ss(tmem + (hf == 0 ? 64u : 192u), sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
+                 sdesc_sw128(k_addr + hf * 16384 + kk * 2048, 16384, 1024), kIdQ, kk > 0);
+      }
+      mma_commit(&sm.dq_full);
+      mma_commit(&sm.q_empty[s]);
+    }
+    mma_commit(&sm.dkv_full);
+    if (!ok) {
+      mma_commit(&sm.drain);
+      int never = 0;
+      mbar_wait(&sm.drain, 0, p.status, &never);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ P / dS, dQ drain, epilogue
+    const int quad = warp % 4;
+    const int jj = quad * 32 + lane;                 // key row in tile == TMEM lane
+    const int key = kv0 + jj;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    uint8_t* ds_row = sm.ds + jj * 128;              // row jj of each 64-query chunk
+    const int swz = jj & 7;
+    bool ok = true;
+    for (int it = 0; it < nq; ++it) {
+      const int s = it & 1;
+      const int q0 = (m_start + it) * kRows;
+      ok = mbar_wait(&sm.q_full[s], (it >> 1) & 1, p.status, abort_flag);
+      ok = ok && mbar_wait(&sm.s_full, it & 1, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = sm.stats[s][0];
+      const float* Dv = sm.stats[s][1];
+      const bool need_mask = (kv0 + kKeys > kvlen) ||
+                             (g.causal && kv0 + kKeys - 1 > g.q_offset + q0);
+      // first query row that sees this key (causal), relative to q0
+      const int first_q = g.causal ? key - g.q_offset - q0 : -(1 << 30);
+      const bool key_ok = key < kvlen;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kRows; c0 += 32) {
+        uint32_t sraw[32], draw[32];
+        tmem_ld32(lane_base + kColS + c0, sraw);
+        tmem_ld32(lane_base + kColDP + c0, draw);
+        tmem_ld_wait();
+        uint32_t pk[16], dk2[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = c0 + 2 * i + e;
+            float pr = ex2(fmaf(__uint_as_float(sraw[2 * i + e]), g.scale_log2, -lse2[c]));
+            if (need_mask && (!key_ok || c < first_q)) pr = 0.0f;
+            pv[e] = pr;
+            dsv[e] = pr * (__uint_as_float(draw[2 * i + e]) - Dv[c]);
+          }
+          pk[i] = pack_bf16x2(pv[0], pv[1]);
+          dk2[i] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        tmem_st16(lane_base + kColS + c0 / 2, pk);
+        tmem_st16(lane_base + kColDP + c0 / 2, dk2);
+        // dS row into the swizzled [key][query] tile: 4 x 16-byte units
+        const int chunk = c0 / 64;
+        const int u0 = (c0 % 64) / 8;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4* dst = reinterpret_cast<uint4*>(ds_row + chunk * 16384 + (((u0 + u) ^ swz) * 16));
+          *dst = make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full);
+      // dQ_i = dS K is ready: lane jj now holds query row q0 + jj
+      ok = mbar_wait(&sm.dq_full, it & 1, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float* dst = p.dq_acc + (static_cast<int64_t>(bh) * p.rows + q0 + jj) * D;
+#pragma unroll
+      for (int hf = 0; hf < kChunks; ++hf) {
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + (hf == 0 ? 64u : 192u) + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            red_add_v4(dst + hf * 64 + c + e, __uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                       __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.dq_empty);
+    }
+    // epilogue: dK = scale * acc, dV = acc (zero when no query row sees this key block)
+    const bool have = nq > 0;
+    if (have && ok) {
+      ok = mbar_wait(&sm.dkv_full, 0, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) tc_fence_after();
+    }
+    const bool store = key < g.sk;
+    __nv_bfloat16* dk_row = p.dk + b * p.k_stride[0] + static_cast<int64_t>(key) * p.k_stride[1] +
+                            h * p.k_stride[2];
+    __nv_bfloat16* dv_row = p.dv + b * p.v_stride[0] + static_cast<int64_t>(key) * p.v_stride[1] +
+                            h * p.v_stride[2];
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t col = which == 0 ? kColDK : kColDV;
+      const float mul = which == 0 ? g.scale : 1.0f;
+      __nv_bfloat16* row = which == 0 ? dk_row : dv_row;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        if (have && ok) {
+          tmem_ld32(lane_base + col + c, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        if (store) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+          uint4* dst = reinterpret_cast<uint4*>(row + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
+  const AttnGeom& g = a.g;
+  const int64_t rows = padded_rows(g.sq);
+  const int64_t bh = static_cast<int64_t>(g.B) * g.H;
+  if (bh == 0 || (g.sq == 0 && g.sk == 0)) return cudaSuccess;
+  cudaError_t e;
+  // 1. statistics + zero the dQ accumulator
+  {
+    const int64_t warps = bh * rows;
+    const int64_t blocks = (warps * 32 + 255) / 256;
+    if (blocks > 0) {
+      if (g.d == 128)
+        bwd_prep_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout),
+            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats, a.dq_acc, g.B, g.H,
+            g.sq, rows);
+      else
+        bwd_prep_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout),
+            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats, a.dq_acc, g.B, g.H,
+            g.sq, rows);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  // 2. main kernel
+  {
+    BwdKernelParams p;
+    p.tq = a.tq;
+    p.tk = a.tk;
+    p.tv = a.tv;
+    p.tdo = a.tdo;
+    p.stats = a.row_stats;
+    p.dq_acc = a.dq_acc;
+    p.dk = static_cast<__nv_bfloat16*>(a.dk);
+    p.dv = static_cast<__nv_bfloat16*>(a.dv);
+    for (int i = 0; i < 3; ++i) {
+      p.k_stride[i] = a.k_stride[i];
+      p.v_stride[i] = a.v_stride[i];
+    }
+    p.g = g;
+    p.rows = rows;
+    p.num_kv_tiles = (g.sk + kKeys - 1) / kKeys;
+    p.status = a.status;
+    const int64_t nblocks = bh * p.num_kv_tiles;
+    if (nblocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (nblocks > 0) {
+      if (g.d == 128) {
+        const size_t smem = sizeof(BwdSmem<128>);
+        if ((e = cudaFuncSetAttribute(attn_bwd_kernel<128>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+            cudaSuccess)
+          return e;
+        attn_bwd_kernel<128><<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(p);
+      } else {
+        const size_t smem = sizeof(BwdSmem<64>);
+        if ((e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+            cudaSuccess)
+          return e;
+        attn_bwd_kernel<64><<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(p);
+      }
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  // 3. dQ convert
+  {
+    const int64_t threads = bh * g.sq * (g.d / 8);
+    const int64_t blocks = (threads + 255) / 256;
+    if (blocks > 0) {
+      if (g.d == 128)
+        bwd_dq_convert_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.q_stride[0], a.q_stride[1],
+            a.q_stride[2], g.B, g.H, g.sq, rows, g.scale);
+      else
+        bwd_dq_convert_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.q_stride[0], a.q_stride[1],
+            a.q_stride[2], g.B, g.H, g.sq, rows, g.scale);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
+}
+
+}  // namespace sp

@@ -1,0 +1,374 @@
+// attn_fwd.cu -- causal / key-padded multi-head attention forward on tcgen05.
+//
+// What it computes ("adv07: Sequence Parallel" tutorial, section 3 Q4 and
+// section 4; "Parallel multi-head attention", section 3.2):
+//     out[i] = softmax(scale * q[i] K^T + mask) V,   lse[i] = log sum_j exp(scale q[i].k_j)
+// over the visible keys j (j <= q_offset + i when causal, j < key_len[b]).
+//
+// Design (one CTA = two 128-row query tiles of one (batch entry, head)):
+//   warp 0        TMA producer: Q tiles once, then K/V blocks through a 2-stage ring
+//   warp 1        MMA issuer (one thread) and TMEM owner
+//   warps 4..7    softmax for query tile 0, warps 8..11 for query tile 1
+//                 (thread = one query row = one TMEM lane)
+// TMEM (512 columns): S0 | S1 | O0 | O1.  S_t = Q_t K_j^T lands in fp32; the
+// softmax warps overwrite its first half with P_t in bf16, which feeds
+// O_t += P_t V_j as the TMEM A operand.  The MMA thread interleaves the two
+// tiles (PV0, next S0, PV1, next S1) so the tensor core works on one tile
+// while the softmax warps of the other tile run.
+// Online softmax in base 2 with fp32 running max m and sum l; O is rescaled
+// in TMEM only when the max grows by more than 2^8 (the stale max keeps P <= 256,
+// and O, l share it, so the final O / l is unchanged).
+// KV blocks past the causal diagonal or past key_len are never loaded; only
+// the blocks that straddle a boundary are masked element-wise.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sp {
+namespace {
+
+constexpr int kRows = 128;      // query rows per tile (TMEM lanes)
+constexpr int kKeys = 128;      // keys per KV block
+constexpr int kStages = 2;
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTileBytes = kRows * D * 2;     // D/64 chunks of [128][64] bf16
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t k[kStages][kTileBytes];
+  alignas(1024) uint8_t v[kStages][kTileBytes];
+  uint64_t q_full;
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct FwdKernelParams {
+  CUtensorMap tq, tk, tv;
+  __nv_bfloat16* o;
+  int64_t o_stride[3];
+  float* lse;
+  AttnGeom g;
+  int num_pairs;      // ceil(sq / 256)
+  uint32_t* status;
+};
+
+struct TileInfo {
+  int q0;        // first query row of the tile
+  int nblocks;   // KV blocks it needs
+};
+
+__device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
+  int n = g.sk;
+  if (g.key_len != nullptr) n = min(n, max(__ldg(g.key_len + b), 0));
+  return n;
+}
+
+__device__ __forceinline__ TileInfo tile_info(const AttnGeom& g, int kvlen, int q0) {
+  TileInfo t{q0, 0};
+  if (q0 >= g.sq) return t;
+  int end = kvlen;
+  if (g.causal) end = min(end, g.q_offset + q0 + kRows);
+  t.nblocks = end > 0 ? (end + kKeys - 1) / kKeys : 0;
+  return t;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdKernelParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(smem_raw);
+  constexpr int kChunks = D / 64;
+  constexpr uint32_t kTileBytes = FwdSmem<D>::kTileBytes;
+  constexpr uint32_t kOCol0 = 256;   // O_t at column 256 + t*D
+
+  const AttnGeom& g = p.g;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int bh = blockIdx.x % (g.B * g.H);
+  const int pair = p.num_pairs - 1 - blockIdx.x / (g.B * g.H);   // heavy (late) tiles first
+  const int b = bh / g.H, h = bh % g.H;
+  const int kvlen = kv_limit(g, b);
+  const TileInfo ti[2] = {tile_info(g, kvlen, pair * 2 * kRows),
+                          tile_info(g, kvlen, pair * 2 * kRows + kRows)};
+  const int nmax = max(ti[0].nblocks, ti[1].nblocks);
+
+  if (threadIdx.x == 0) {
+    if ((smem_u32(smem_raw) & 1023u) != 0) raise_status(p.status, kStatusBadSmem);
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], kRows);
+    }
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == 0 && lane == 0 && nmax > 0) {
+    // ------------------------------------------------------------ TMA producer
+    tma_prefetch_desc(&p.tq);
+    tma_prefetch_desc(&p.tk);
+    tma_prefetch_desc(&p.tv);
+    const int ntiles = ti[1].nblocks > 0 ? 2 : 1;
+    mbar_expect_tx(&sm.q_full, kTileBytes * ntiles);
+    for (int t = 0; t < ntiles; ++t)
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_4d(sm.q[t] + c * 16384, &p.tq, &sm.q_full, c * 64, h, ti[t].q0, b);
+    for (int j = 0; j < nmax; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages && !mbar_wait(&sm.kv_empty[s], ((j / kStages) - 1) & 1, p.status, abort_flag))
+        break;
+      mbar_expect_tx(&sm.k_full[s], kTileBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_4d(sm.k[s] + c * 16384, &p.tk, &sm.k_full[s], c * 64, h, j * kKeys, b);
+      mbar_expect_tx(&sm.v_full[s], kTileBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_4d(sm.v[s] + c * 16384, &p.tv, &sm.v_full[s], c * 64, h, j * kKeys, b);
+    }
+  } else if (warp == 1 && lane == 0 && nmax > 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16(kRows, kKeys, false, false);
+    constexpr uint32_t kIdO = idesc_bf16(kRows, D, false, true);
+    const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+    int k_ready = -1;   // highest KV block whose K tile has been waited for
+    bool ok = mbar_wait(&sm.q_full, 0, p.status, abort_flag);
+    auto ensure_k = [&](int j) -> bool {
+      if (k_ready >= j) return true;
+      k_ready = j;
+      const bool r = mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, p.status, abort_flag);
+      tc_fence_after();
+      return r;
+    };
+    auto issue_s = [&](int t, int j) {
+      const uint32_t k_addr = smem_u32(sm.k[j % kStages]);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+        mma_ss(tmem + t * kKeys, sdesc_sw128(q_addr[t] + off, 16, 1024),
+               sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
+      }
+      mma_commit(&sm.s_full[t]);
+    };
+    auto issue_pv = [&](int t, int j) {
+      const uint32_t v_addr = smem_u32(sm.v[j % kStages]);
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk)
+        mma_ts(tmem + kOCol0 + t * D, tmem + t * kKeys + kk * 8,
+               sdesc_sw128(v_addr + kk * 2048, 16384, 1024), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    if (ok) {
+      tc_fence_after();
+      ok = ensure_k(0);
+      for (int t = 0; t < 2 && ok; ++t)
+        if (ti[t].nblocks > 0) issue_s(t, 0);
+    }
+    for (int j = 0; j < nmax && ok; ++j) {
+      const int s = j % kStages;
+      if (!(ok = mbar_wait(&sm.v_full[s], (j / kStages) & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      // tile 0
+      if (j < ti[0].nblocks) {
+        if (!(ok = mbar_wait(&sm.p_full[0], j & 1, p.status, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(0, j);
+      }
+      if (j + 1 < ti[0].nblocks) {
+        if (!(ok = ensure_k(j + 1))) break;
+        issue_s(0, j + 1);
+      }
+      // tile 1
+      if (j < ti[1].nblocks) {
+        if (!(ok = mbar_wait(&sm.p_full[1], j & 1, p.status, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(1, j);
+      }
+      mma_commit(&sm.kv_empty[s]);
+      if (j + 1 < ti[1].nblocks) {
+        if (!(ok = ensure_k(j + 1))) break;
+        issue_s(1, j + 1);
+      }
+    }
+    mma_commit(&sm.o_full);
+    if (!ok) {
+      // unwinding: let every issued MMA finish before TMEM is released
+      mma_commit(&sm.drain);
+      int never = 0;
+      mbar_wait(&sm.drain, 0, p.status, &never);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = (warp - 4) / 4;
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;                  // row in tile == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t s_col = t * kKeys;
+    const uint32_t o_col = kOCol0 + t * D;
+    const TileInfo tile = ti[t];
+    const int qrow = tile.q0 + r;                    // local query row
+    const int gq = g.q_offset + qrow;                // global position (causal mask)
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < tile.nblocks; ++j) {
+      if (!(ok = mbar_wait(&sm.s_full[t], j & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      float sv[kKeys];
+#pragma unroll
+      for (int c = 0; c < kKeys / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld32(lane_base + s_col + c * 32, raw);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(raw[i]);
+      }
+      const int key0 = j * kKeys;
+      const bool need_mask = (key0 + kKeys > kvlen) ||
+                             (g.causal && key0 + kKeys - 1 > g.q_offset + tile.q0);
+      if (need_mask) {
+        const int lim = g.causal ? min(kvlen, gq + 1) : kvlen;   // visible keys: key < lim
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c)
+          if (key0 + c >= lim) sv[c] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < kKeys; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_blk = mx * g.scale_log2;
+      float m_use = m;
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (j == 0) {
+        m_use = m_blk;
+      } else if (m_blk > m + kRescaleThreshold) {
+        m_use = m_blk;
+        alpha = ex2(m - m_blk);
+        rescale = true;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O_t += P V of block j-1 has completed (it precedes this S in issue order)
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t ov[16];
+          tmem_ld16(lane_base + o_col + c * 16, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st16(lane_base + o_col + c * 16, ov);
+        }
+        tmem_st_wait();
+      }
+      l *= alpha;
+      m = m_use;
+      const float neg_m = -m;
+#pragma unroll
+      for (int c = 0; c < kKeys / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(sv[c * 32 + 2 * i], g.scale_log2, neg_m));
+          const float p1 = ex2(fmaf(sv[c * 32 + 2 * i + 1], g.scale_log2, neg_m));
+          l += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(lane_base + s_col + c * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[t]);
+    }
+    // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
+    if (qrow < g.sq) {
+      __nv_bfloat16* orow = p.o + b * p.o_stride[0] + static_cast<int64_t>(qrow) * p.o_stride[1] +
+                            h * p.o_stride[2];
+      float* lse_out = p.lse + (static_cast<int64_t>(b) * g.H + h) * g.sq + qrow;
+      if (tile.nblocks == 0 || !ok) {
+        uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+        *lse_out = -INFINITY;
+      }
+    }
+    if (tile.nblocks > 0 && ok) {
+      ok = mbar_wait(&sm.o_full, 0, p.status, abort_flag);
+      tc_fence_after();
+      const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(lane_base + o_col + c * 32, ov);
+        tmem_ld_wait();
+        if (qrow < g.sq && ok) {
+          __nv_bfloat16* orow = p.o + b * p.o_stride[0] +
+                                static_cast<int64_t>(qrow) * p.o_stride[1] + h * p.o_stride[2];
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                __uint_as_float(ov[2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (qrow < g.sq && ok) {
+        float* lse_out = p.lse + (static_cast<int64_t>(b) * g.H + h) * g.sq + qrow;
+        *lse_out = (m + __log2f(l)) * 0.69314718055994531f;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
+  FwdKernelParams p;
+  p.tq = a.tq;
+  p.tk = a.tk;
+  p.tv = a.tv;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  for (int i = 0; i < 3; ++i) p.o_stride[i] = a.o_stride[i];
+  p.lse = a.lse;
+  p.g = a.g;
+  p.num_pairs = (a.g.sq + 2 * kRows - 1) / (2 * kRows);
+  p.status = a.status;
+  const int64_t nblocks = static_cast<int64_t>(p.num_pairs) * a.g.B * a.g.H;
+  if (nblocks == 0) return cudaSuccess;
+  if (nblocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  if (a.g.d == 128) {
+    const size_t smem = sizeof(FwdSmem<128>);
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_fwd_kernel<128><<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(p);
+  } else {
+    const size_t smem = sizeof(FwdSmem<64>);
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attn_fwd_kernel<64><<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sp

@@ -1,0 +1,266 @@
+// sp_abi.cu -- the extern "C" boundary of libsp (declared in include/sp.h).
+//
+// Every entry point validates its arguments on the host and returns before
+// launching anything when they are wrong.  The only library-held device state
+// is a 4-byte status word that kernels OR error codes into (read and cleared by
+// sp_get_device_status).
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sp {
+
+__device__ uint32_t g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint32_t*> g_status_addr[kMaxDevices];
+
+// Device address of the status word for the current device (looked up once per device).
+uint32_t* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  uint32_t* a = g_status_addr[dev].load(std::memory_order_acquire);
+  if (a == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    a = static_cast<uint32_t*>(p);
+    g_status_addr[dev].store(a, std::memory_order_release);
+  }
+  return a;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sp_status check_relayout(const void* const* in, void* const* out, int ntensors, int N, int b,
+                         int s, int h, int d) {
+  if (in == nullptr || out == nullptr) return SP_ERR_INVALID_ARG;
+  if (ntensors < 1 || ntensors > SP_MAX_RELAYOUT_TENSORS) return SP_ERR_INVALID_ARG;
+  if (N < 1 || b < 1 || s < 1 || h < 1 || d < 1) return SP_ERR_INVALID_ARG;
+  if (s % N != 0 || h % N != 0) return SP_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(b) * s * h * d > (int64_t(1) << 40)) return SP_ERR_UNSUPPORTED;
+  for (int t = 0; t < ntensors; ++t) {
+    if (in[t] == nullptr || out[t] == nullptr) return SP_ERR_INVALID_ARG;
+    if (!aligned16(in[t]) || !aligned16(out[t])) return SP_ERR_MISALIGNED;
+  }
+  return SP_OK;
+}
+
+sp_status relayout(const void* const* in, void* const* out, int ntensors, int N, int b, int s,
+                   int h, int d, bool to_heads, void* stream) {
+  const sp_status st = check_relayout(in, out, ntensors, N, b, s, h, d);
+  if (st != SP_OK) return st;
+  if (launch_relayout(in, out, ntensors, N, b, s, h, d, to_heads,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SP_ERR_CUDA;
+  return SP_OK;
+}
+
+bool strides_ok(const int64_t st[3]) {
+  for (int i = 0; i < 3; ++i)
+    if (st[i] < 0 || (st[i] % 8) != 0) return false;
+  return true;
+}
+
+sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
+  if (p == nullptr) return SP_ERR_INVALID_ARG;
+  if (p->B < 0 || p->H < 0 || p->sq < 0 || p->sk < 0) return SP_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return SP_ERR_INVALID_ARG;
+  if (p->q_offset < 0) return SP_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return SP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->q_offset) + p->sq > (int64_t(1) << 30)) return SP_ERR_UNSUPPORTED;
+  if (p->q == nullptr || p->k == nullptr || p->v == nullptr) return SP_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v)) return SP_ERR_MISALIGNED;
+  if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride) || !strides_ok(p->v_stride) ||
+      !strides_ok(p->o_stride))
+    return SP_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(p->key_len) & 3u) != 0) return SP_ERR_MISALIGNED;
+  g->B = p->B;
+  g->H = p->H;
+  g->sq = p->sq;
+  g->sk = p->sk;
+  g->d = p->d;
+  g->causal = p->causal;
+  g->q_offset = p->q_offset;
+  g->key_len = p->key_len;
+  float scale = p->softmax_scale;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(p->d));
+  g->scale = scale;
+  g->scale_log2 = scale * 1.4426950408889634f;
+  return SP_OK;
+}
+
+bool empty_problem(const AttnGeom& g) { return g.B == 0 || g.H == 0 || g.sq == 0; }
+
+struct WorkspaceLayout {
+  size_t dq_off, stats_off, total;
+};
+
+WorkspaceLayout workspace_layout(const AttnGeom& g) {
+  const size_t bh = static_cast<size_t>(g.B) * g.H;
+  const size_t rows = static_cast<size_t>(padded_rows(g.sq));
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  WorkspaceLayout w;
+  w.dq_off = 0;
+  w.stats_off = up(bh * rows * g.d * sizeof(float));
+  w.total = w.stats_off + up(bh * 2 * rows * sizeof(float));
+  return w;
+}
+
+}  // namespace
+
+bool encode_rows_map(CUtensorMap* map, const void* base, int d, int S, int H, int B,
+                     const int64_t stride[3]) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t legal = static_cast<cuuint64_t>(d) * 2;   // any 16-byte multiple works for size-1 dims
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H > 0 ? H : 1),
+                        static_cast<cuuint64_t>(S > 0 ? S : 1), static_cast<cuuint64_t>(B > 0 ? B : 1)};
+  cuuint64_t strides[3] = {H > 1 ? static_cast<cuuint64_t>(stride[2]) * 2 : legal,
+                           S > 1 ? static_cast<cuuint64_t>(stride[1]) * 2 : legal,
+                           B > 1 ? static_cast<cuuint64_t>(stride[0]) * 2 : legal};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t elem[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace sp
+
+using namespace sp;
+
+extern "C" {
+
+sp_status sp_relayout_seq2head(const void* const* in, void* const* out, int ntensors, int N,
+                               int b, int s, int h, int d, void* stream) {
+  return relayout(in, out, ntensors, N, b, s, h, d, true, stream);
+}
+
+sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int ntensors, int N,
+                               int b, int s, int h, int d, void* stream) {
+  return relayout(in, out, ntensors, N, b, s, h, d, false, stream);
+}
+
+sp_status sp_attn_fwd(const sp_attn_params* p, void* o, float* lse, void* stream) {
+  AttnGeom g;
+  sp_status st = check_attn(p, &g);
+  if (st != SP_OK) return st;
+  if (o == nullptr || lse == nullptr) return SP_ERR_INVALID_ARG;
+  if (!aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return SP_ERR_MISALIGNED;
+  if (empty_problem(g)) return SP_OK;
+  FwdArgs a;
+  if (!encode_rows_map(&a.tq, p->q, g.d, g.sq, g.H, g.B, p->q_stride) ||
+      !encode_rows_map(&a.tk, p->k, g.d, g.sk, g.H, g.B, p->k_stride) ||
+      !encode_rows_map(&a.tv, p->v, g.d, g.sk, g.H, g.B, p->v_stride))
+    return SP_ERR_CUDA;
+  a.o = o;
+  for (int i = 0; i < 3; ++i) a.o_stride[i] = p->o_stride[i];
+  a.lse = lse;
+  a.g = g;
+  a.status = status_word();
+  if (a.status == nullptr) return SP_ERR_CUDA;
+  return launch_attn_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+size_t sp_attn_bwd_workspace_size(const sp_attn_params* p) {
+  AttnGeom g;
+  if (check_attn(p, &g) != SP_OK) return 0;
+  return workspace_layout(g).total;
+}
+
+sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, const void* dout,
+                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  AttnGeom g;
+  sp_status st = check_attn(p, &g);
+  if (st != SP_OK) return st;
+  if (o == nullptr || lse == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||
+      dv == nullptr)
+    return SP_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return SP_ERR_MISALIGNED;
+  if (g.B == 0 || g.H == 0) return SP_OK;
+  const WorkspaceLayout w = workspace_layout(g);
+  if (workspace == nullptr || workspace_bytes < w.total) return SP_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SP_ERR_MISALIGNED;
+  BwdArgs a;
+  if (g.sq > 0 && g.sk > 0) {
+    if (!encode_rows_map(&a.tq, p->q, g.d, g.sq, g.H, g.B, p->q_stride) ||
+        !encode_rows_map(&a.tk, p->k, g.d, g.sk, g.H, g.B, p->k_stride) ||
+        !encode_rows_map(&a.tv, p->v, g.d, g.sk, g.H, g.B, p->v_stride) ||
+        !encode_rows_map(&a.tdo, dout, g.d, g.sq, g.H, g.B, p->o_stride))
+      return SP_ERR_CUDA;
+  }
+  a.o = o;
+  a.dout = dout;
+  for (int i = 0; i < 3; ++i) {
+    a.o_stride[i] = p->o_stride[i];
+    a.q_stride[i] = p->q_stride[i];
+    a.k_stride[i] = p->k_stride[i];
+    a.v_stride[i] = p->v_stride[i];
+  }
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.dq_off);
+  a.row_stats = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.stats_off);
+  a.g = g;
+  a.status = status_word();
+  if (a.status == nullptr) return SP_ERR_CUDA;
+  return launch_attn_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+sp_status sp_get_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SP_ERR_CUDA;
+  uint32_t* addr = status_word();
+  if (addr == nullptr) return SP_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, addr, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SP_ERR_CUDA;
+  if (cudaMemsetAsync(addr, 0, sizeof word, s) != cudaSuccess) return SP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SP_ERR_CUDA;
+  if (word & kStatusTimeout) return SP_ERR_TIMEOUT;
+  if (word != 0) return SP_ERR_CUDA;
+  return SP_OK;
+}
+
+const char* sp_status_string(sp_status s) {
+  switch (s) {
+    case SP_OK: return "ok";
+    case SP_ERR_INVALID_ARG: return "invalid argument";
+    case SP_ERR_UNSUPPORTED: return "unsupported problem";
+    case SP_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case SP_ERR_CUDA: return "CUDA error";
+    case SP_ERR_TIMEOUT: return "device-side wait timed out";
+    case SP_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

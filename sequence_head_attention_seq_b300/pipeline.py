@@ -1,0 +1,90 @@
+"""The Ulysses attention step on one GPU, as a sequence of libsp calls.
+
+forward  : Q/K/V shards --seq2head--> head groups --attn_fwd--> O groups --head2seq--> O shards
+backward : dO shards --seq2head--> dO groups --attn_bwd--> dQ/dK/dV groups --head2seq--> shards
+
+Shards are [N][b][s/N][h][d] and groups [N][b][s][h/N][d]; attention runs once over
+all groups, viewed as N*b batch entries of h/N heads (heads are independent,
+"Parallel multi-head attention" section 2).  Buffers are allocated once (torch) and
+reused by every step.
+"""
+from __future__ import annotations
+
+import contextlib
+
+import torch
+
+from .binding import (sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd,
+                      sp_relayout_head2seq, sp_relayout_seq2head)
+
+
+class UlyssesAttention:
+    def __init__(self, N: int, b: int, s: int, h: int, d: int, causal: bool = True,
+                 key_len: torch.Tensor | None = None, softmax_scale: float | None = None,
+                 device="cuda", timer=None):
+        """`timer(name)`, if given, returns a context manager wrapped around each
+        library call (used to bracket calls with CUDA events)."""
+        if s % N or h % N:
+            raise ValueError("s and h must be divisible by N")
+        self.N, self.b, self.s, self.h, self.d = N, b, s, h, d
+        self.causal = causal
+        self.softmax_scale = softmax_scale
+        self.timer = timer if timer is not None else (lambda name: contextlib.nullcontext())
+        dev = torch.device(device)
+        hl = h // N
+        gshape = (N, b, s, hl, d)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        # key lengths per batch row, repeated for every head group (batch entry g*b + bb)
+        self.key_len = None if key_len is None else key_len.to(dev, torch.int32).repeat(N)
+        self.qg, self.kg, self.vg = (torch.empty(gshape, **bf) for _ in range(3))
+        self.og = torch.empty(gshape, **bf)
+        self.dog = torch.empty(gshape, **bf)
+        self.dqg, self.dkg, self.dvg = (torch.empty(gshape, **bf) for _ in range(3))
+        self.lse = torch.empty((N * b, hl, s), dtype=torch.float32, device=dev)
+        sshape = (N, b, s // N, h, d)
+        self.o = torch.empty(sshape, **bf)
+        self.dq, self.dk, self.dv = (torch.empty(sshape, **bf) for _ in range(3))
+        ws = sp_attn_bwd_workspace_size(self._g(self.qg), self._g(self.kg), self._g(self.vg),
+                                        causal, 0, self.key_len, softmax_scale)
+        self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+
+    def _g(self, t: torch.Tensor) -> torch.Tensor:
+        """Group buffer [N][b][s][hl][d] viewed as attention batch [N*b][s][hl][d]."""
+        return t.view(self.N * self.b, self.s, self.h // self.N, self.d)
+
+    def _to_groups(self, shards, groups, name):
+        if self.N == 1:
+            for x, y in zip(shards, groups):
+                y.copy_(x)          # one shard is already the full sequence
+            return
+        with self.timer(name):
+            sp_relayout_seq2head(list(shards), self.N, outs=list(groups))
+
+    def _to_shards(self, groups, shards, name):
+        if self.N == 1:
+            for x, y in zip(groups, shards):
+                y.copy_(x)
+            return
+        with self.timer(name):
+            sp_relayout_head2seq(list(groups), self.N, outs=list(shards))
+
+    def forward(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> torch.Tensor:
+        """q, k, v: [N][b][s/N][h][d] shards -> O shards (same layout)."""
+        self._to_groups((q, k, v), (self.qg, self.kg, self.vg), "seq2head_qkv")
+        with self.timer("attn_fwd"):
+            sp_attn_fwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self.causal, 0,
+                        self.key_len, self.softmax_scale, out=self._g(self.og), lse=self.lse)
+        self._to_shards((self.og,), (self.o,), "head2seq_o")
+        return self.o
+
+    def backward(self, dout: torch.Tensor):
+        """dout shards -> (dq, dk, dv) shards; uses the last forward's O and lse."""
+        self._to_groups((dout,), (self.dog,), "seq2head_do")
+        with self.timer("attn_bwd"):
+            sp_attn_bwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self._g(self.og),
+                        self.lse, self._g(self.dog), self.causal, 0, self.key_len,
+                        self.softmax_scale, dq=self._g(self.dqg), dk=self._g(self.dkg),
+                        dv=self._g(self.dvg), workspace=self.workspace)
+        self._to_shards((self.dqg, self.dkg, self.dvg), (self.dq, self.dk, self.dv),
+                        "head2seq_grads")
+        return self.dq, self.dk, self.dv

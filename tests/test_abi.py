@@ -1,0 +1,136 @@
+"""Host-only checks of the C ABI: the library builds and loads without a GPU,
+exports exactly what include/sp.h declares, and rejects bad arguments before
+launching anything (fake, never-dereferenced pointers are enough for that)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sequence_head_attention_seq_b300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sp.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA, TIMEOUT, WORKSPACE = range(7)
+FAKE = 0x10000          # 16-byte aligned, never dereferenced
+FAKE_ODD = 0x10008      # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_binding_exports():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(sp_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_build_targets_sm_103a_only():
+    from sequence_head_attention_seq_b300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert binding.sp_status_string(code)
+    assert binding.sp_status_string(99) == "unknown status"
+
+
+def _arr(*vals):
+    a = (ctypes.c_void_p * len(vals))(*vals)
+    return ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)), a
+
+
+@pytest.mark.parametrize("fn", ["sp_relayout_seq2head", "sp_relayout_head2seq"])
+def test_relayout_validation(lib, fn):
+    f = getattr(lib, fn)
+    pin, a = _arr(FAKE, FAKE)
+    pout, b = _arr(FAKE * 2, FAKE * 3)
+    assert f(pin, pout, 2, 0, 1, 8, 4, 64, None) == INVALID          # N < 1
+    assert f(pin, pout, 2, 3, 1, 8, 3, 64, None) == INVALID          # s % N
+    assert f(pin, pout, 2, 2, 1, 8, 3, 64, None) == INVALID          # h % N
+    assert f(pin, pout, 0, 2, 1, 8, 4, 64, None) == INVALID          # ntensors
+    assert f(pin, pout, 9, 2, 1, 8, 4, 64, None) == INVALID
+    assert f(None, pout, 2, 2, 1, 8, 4, 64, None) == INVALID
+    pnull, c = _arr(FAKE, 0)
+    assert f(pnull, pout, 2, 2, 1, 8, 4, 64, None) == INVALID
+    podd, e = _arr(FAKE, FAKE_ODD)
+    assert f(podd, pout, 2, 2, 1, 8, 4, 64, None) == MISALIGNED
+
+
+def _params(**kw):
+    p = binding.SpAttnParams()
+    p.q = p.k = p.v = FAKE
+    for name in ("q_stride", "k_stride", "v_stride", "o_stride"):
+        setattr(p, name, (ctypes.c_int64 * 3)(128 * 256 * 4, 128 * 4, 128))
+    p.B, p.H, p.sq, p.sk, p.d = 1, 4, 256, 256, 128
+    p.causal, p.q_offset = 1, 0
+    p.key_len = None
+    p.softmax_scale = 0.0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), UNSUPPORTED),
+    (dict(d=256), UNSUPPORTED),
+    (dict(causal=2), INVALID),
+    (dict(q_offset=-1), INVALID),
+    (dict(sq=-1), INVALID),
+    (dict(B=-2), INVALID),
+    (dict(q=None), INVALID),
+    (dict(k=FAKE_ODD), MISALIGNED),
+    (dict(q_stride=(ctypes.c_int64 * 3)(4, 4, 4)), MISALIGNED),
+    (dict(key_len=FAKE + 2), MISALIGNED),
+])
+def test_attn_validation(lib, kw, code):
+    p = _params(**kw)
+    assert lib.sp_attn_fwd(ctypes.byref(p), FAKE, FAKE, None) == code
+    assert lib.sp_attn_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                           1 << 40, None) == code
+    assert lib.sp_attn_bwd_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_attn_output_pointer_validation(lib):
+    p = _params()
+    assert lib.sp_attn_fwd(ctypes.byref(p), None, FAKE, None) == INVALID
+    assert lib.sp_attn_fwd(ctypes.byref(p), FAKE, None, None) == INVALID
+    assert lib.sp_attn_fwd(ctypes.byref(p), FAKE_ODD, FAKE, None) == MISALIGNED
+    assert lib.sp_attn_fwd(None, FAKE, FAKE, None) == INVALID
+
+
+def test_workspace_size_and_check(lib):
+    p = _params(B=2, H=3, sq=200, d=64)
+    rows = 256                                   # 200 rounded up to 128-row tiles
+    up = lambda x: (x + 255) // 256 * 256
+    expect = up(2 * 3 * rows * 64 * 4) + up(2 * 3 * 2 * rows * 4)
+    assert lib.sp_attn_bwd_workspace_size(ctypes.byref(p)) == expect
+    assert lib.sp_attn_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                           expect - 1, None) == WORKSPACE
+    assert lib.sp_attn_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16,
+                           expect, None) == MISALIGNED
+
+
+def test_empty_problems_launch_nothing(lib):
+    # zero batch entries / heads / query rows: nothing to do, SP_OK without touching CUDA
+    for kw in (dict(B=0), dict(H=0), dict(sq=0)):
+        p = _params(**kw)
+        assert lib.sp_attn_fwd(ctypes.byref(p), FAKE, FAKE, None) == OK

@@ -1,0 +1,292 @@
+"""GPU attention forward/backward against the fp64 oracle, on the same seeded
+bf16 inputs.  Small problems are compared element by element over every output;
+the long workloads on sampled rows the oracle computes one by one, plus
+properties that hold at any size."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (check_grad, check_lse, check_out, check_status, f64, need_gpu)
+from sequence_head_attention_seq_b300 import (UlyssesAttention, sp_attn_bwd, sp_attn_fwd,
+                                              sp_relayout_head2seq, workloads)
+
+pytestmark = pytest.mark.gpu
+
+
+def _randn(shape, seed, scale=1.0):
+    return workloads.randn_bf16(shape, seed, scale, device="cuda")
+
+
+def _run(q, k, v, do, causal, q_offset=0, key_len=None):
+    kl = None if key_len is None else torch.tensor(key_len, dtype=torch.int32, device="cuda")
+    o, lse = sp_attn_fwd(q, k, v, causal, q_offset, kl)
+    dq, dk, dv = sp_attn_bwd(q, k, v, o, lse, do, causal, q_offset, kl)
+    torch.cuda.synchronize()
+    check_status()
+    return o, lse, dq, dk, dv
+
+
+SMALL = [
+    # B, H, sq, sk, d, causal, q_offset, key_len
+    (1, 2, 128, 128, 64, True, 0, None),          # one tile pair, half empty
+    (2, 3, 300, 300, 128, True, 0, None),         # ragged tail, 3 query tiles
+    (1, 1, 640, 640, 128, True, 0, None),         # 2.5 tile pairs
+    (4, 2, 257, 257, 64, False, 0, [257, 129, 1, 0]),   # padding, one empty batch entry
+    (2, 2, 200, 456, 128, True, 256, None),       # query shard at an offset
+    (1, 2, 1, 130, 64, True, 129, None),          # a single query row
+    (2, 1, 100, 333, 128, False, 0, [333, 50]),   # non-causal, sq != sk
+    (1, 1, 384, 384, 64, True, 0, [384]),         # causal with an explicit full key_len
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[str(c[:8]) for c in SMALL])
+def test_small_against_oracle(case):
+    need_gpu()
+    B, H, sq, sk, d, causal, q_offset, key_len = case
+    seed = 17 * sq + sk
+    q = _randn((B, sq, H, d), seed)
+    k = _randn((B, sk, H, d), seed + 1)
+    v = _randn((B, sk, H, d), seed + 2)
+    do = _randn((B, sq, H, d), seed + 3)
+    o, lse, dq, dk, dv = _run(q, k, v, do, causal, q_offset, key_len)
+    orc = oracle.default()
+    ro, rl = orc.attn_fwd(f64(q), f64(k), f64(v), causal, q_offset, key_len)
+    rdq, rdk, rdv = orc.attn_bwd(f64(q), f64(k), f64(v), f64(do), causal, q_offset, key_len)
+    check_out(f64(o), ro, "out")
+    check_lse(f64(lse), rl, "lse")
+    check_grad(f64(dq), rdq, "dq")
+    check_grad(f64(dk), rdk, "dk")
+    check_grad(f64(dv), rdv, "dv")
+
+
+def test_causal_row0_returns_v0_bit_exact():
+    need_gpu()
+    q, k, v = (_randn((2, 300, 4, 128), 40 + t) for t in range(3))
+    o, _ = sp_attn_fwd(q, k, v, True)
+    torch.cuda.synchronize()
+    check_status()
+    assert torch.equal(o[:, 0].view(torch.int16), v[:, 0].view(torch.int16))
+
+
+def test_constant_v_gives_constant_out():
+    need_gpu()
+    q, k = _randn((1, 513, 2, 64), 50, 2.0), _randn((1, 513, 2, 64), 51, 2.0)
+    c = _randn((64,), 52)
+    v = c.view(1, 1, 1, 64).expand(1, 513, 2, 64).contiguous()
+    # one bf16 ulp of each c: the weights are applied in bf16 while l sums them in fp32
+    cf = c.float()
+    ulp = torch.exp2(torch.floor(torch.log2(cf.abs())) - 7)
+    for causal in (True, False):
+        o, _ = sp_attn_fwd(q, k, v, causal)
+        torch.cuda.synchronize()
+        assert ((o.float() - cf).abs() <= ulp).all()
+
+
+def test_split_q_identity():
+    """adv07 tutorial section 4: query shards against the full K/V, concatenated,
+    equal unsharded attention.  The forward is bit-identical (every row visits
+    the same key blocks in the same order; extra fully masked blocks add 0)."""
+    need_gpu()
+    s, H, d = 1024, 2, 128
+    q, k, v, do = (_randn((1, s, H, d), 60 + t) for t in range(4))
+    o, lse, dq, dk, dv = _run(q, k, v, do, True)
+    parts = []
+    dk_sum = torch.zeros_like(dk, dtype=torch.float32)
+    dv_sum = torch.zeros_like(dv, dtype=torch.float32)
+    dq_parts = []
+    for lo, hi in ((0, 384), (384, 512), (512, 1024)):
+        so, sl, sdq, sdk, sdv = _run(q[:, lo:hi].contiguous(), k, v, do[:, lo:hi].contiguous(),
+                                     True, q_offset=lo)
+        parts.append(so)
+        dq_parts.append(sdq)
+        dk_sum += sdk.float()
+        dv_sum += sdv.float()
+        assert torch.equal(sl, lse[:, :, lo:hi])
+    assert torch.equal(torch.cat(parts, 1).view(torch.int16), o.view(torch.int16))
+    check_grad(f64(torch.cat(dq_parts, 1)), f64(dq), "dq shards")
+    # shard gradients of K/V add up to the unsharded ones (reduce-scatter semantics)
+    check_grad(dk_sum.double().cpu().numpy(), f64(dk), "dk sum")
+    check_grad(dv_sum.double().cpu().numpy(), f64(dv), "dv sum")
+
+
+def test_own_shard_kv_is_not_attention():
+    """adv07 tutorial section 4: a shard that only sees its own K/V is wrong."""
+    need_gpu()
+    q, k, v = (_randn((1, 256, 1, 64), 70 + t) for t in range(3))
+    full, _ = sp_attn_fwd(q, k, v, True)
+    wrong, _ = sp_attn_fwd(q[:, 128:], k[:, 128:], v[:, 128:], True)
+    torch.cuda.synchronize()
+    assert (wrong.float() - full[:, 128:].float()).abs().max().item() > 0.1
+
+
+def test_key_padding_equals_truncation():
+    need_gpu()
+    q, do = _randn((1, 200, 2, 128), 80), _randn((1, 200, 2, 128), 81)
+    k, v = _randn((1, 400, 2, 128), 82), _randn((1, 400, 2, 128), 83)
+    L = 250
+    o, lse, dq, dk, dv = _run(q, k, v, do, False, key_len=[L])
+    ot, lt, dqt, dkt, dvt = _run(q, k[:, :L].contiguous(), v[:, :L].contiguous(), do, False)
+    assert torch.equal(o.view(torch.int16), ot.view(torch.int16))
+    assert torch.equal(lse, lt)
+    check_grad(f64(dq), f64(dqt), "dq")
+    check_grad(f64(dk[:, :L]), f64(dkt), "dk")
+    assert not dk[:, L:].any() and not dv[:, L:].any()
+
+
+def test_empty_rows():
+    need_gpu()
+    q, do = _randn((2, 130, 1, 64), 90), _randn((2, 130, 1, 64), 91)
+    k, v = _randn((2, 140, 1, 64), 92), _randn((2, 140, 1, 64), 93)
+    o, lse, dq, dk, dv = _run(q, k, v, do, False, key_len=[0, 140])
+    assert not o[0].any() and torch.all(lse[0] == -math.inf)
+    assert not dq[0].any() and not dk[0].any() and not dv[0].any()
+
+
+def test_repeat_calls_are_deterministic_forward():
+    need_gpu()
+    q, k, v = (_randn((1, 700, 3, 128), 95 + t) for t in range(3))
+    a, la = sp_attn_fwd(q, k, v, True)
+    b, lb = sp_attn_fwd(q, k, v, True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16)) and torch.equal(la, lb)
+
+
+# ---------------------------------------------------------------- the workloads
+
+def _oracle_group_inputs(w, ins, orc):
+    """The oracle's own seq->head regrouping of the shard inputs (fp64 per group)."""
+    out = {}
+    for name in ("q", "k", "v", "dout"):
+        bits = ins[name].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+        grp = orc.seq2head(bits, w.N, w.b, w.s, w.h, w.d)        # [N][b][s][hl][d]
+        out[name] = grp
+    return out
+
+
+def _bits_to_f64(a: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _head(grp, gi, bb, j):
+    """[s][d] of head group gi, batch row bb, local head j -> oracle layout [1][s][1][d]."""
+    x = grp[gi, bb, :, j, :]
+    return _bits_to_f64(x)[None, :, None, :]
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama7b", "padded"])
+def test_workload_full_heads(name):
+    """Whole Ulysses step; sampled heads compared over every row and column."""
+    need_gpu()
+    w = workloads.WORKLOADS[name]
+    ins = workloads.make_inputs(w, device="cuda")
+    kl = ins["key_len"]
+    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=kl)
+    o = step.forward(ins["q"], ins["k"], ins["v"]).clone()
+    dq, dk, dv = (t.clone() for t in step.backward(ins["dout"]))
+    torch.cuda.synchronize()
+    check_status()
+    orc = oracle.default()
+    grp = _oracle_group_inputs(w, ins, orc)
+    # the outputs came back through head->seq: regroup them with the oracle to index heads
+    og = orc.seq2head(o.cpu().view(torch.int16).numpy().view(np.uint16), w.N, w.b, w.s, w.h, w.d)
+    dqg, dkg, dvg = (orc.seq2head(t.cpu().view(torch.int16).numpy().view(np.uint16),
+                                  w.N, w.b, w.s, w.h, w.d) for t in (dq, dk, dv))
+    heads = {(0, 0, 0), (w.N - 1, w.b - 1, w.h_local - 1)}
+    if name == "tiny":
+        heads = {(g, 0, 0) for g in range(w.N)}
+    for gi, bb, j in sorted(heads):
+        args = [_head(grp[n], gi, bb, j) for n in ("q", "k", "v", "dout")]
+        key_len = None if kl is None else [int(kl[bb])]
+        ro, rl = orc.attn_fwd(*args[:3], w.causal, 0, key_len)
+        rdq, rdk, rdv = orc.attn_bwd(*args, w.causal, 0, key_len)
+        tag = f"{name} group {gi} batch {bb} head {j}"
+        check_out(_bits_to_f64(og[gi, bb, :, j])[None, :, None, :], ro, tag + " out")
+        lse = step.lse[gi * w.b + bb, j].double().cpu().numpy()
+        check_lse(lse[None, None, :], rl, tag + " lse")
+        check_grad(_bits_to_f64(dqg[gi, bb, :, j])[None, :, None, :], rdq, tag + " dq")
+        check_grad(_bits_to_f64(dkg[gi, bb, :, j])[None, :, None, :], rdk, tag + " dk")
+        check_grad(_bits_to_f64(dvg[gi, bb, :, j])[None, :, None, :], rdv, tag + " dv")
+    _check_gradient_sums(step, w)
+    if name == "tiny":
+        _check_tiny_split_q(w, ins)
+
+
+def _check_gradient_sums(step, w):
+    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per head, over every head (rows with keys)."""
+    dk = step.dkg.float().view(w.N * w.b, w.s, w.h_local, w.d)
+    dv = step.dvg.float().view(w.N * w.b, w.s, w.h_local, w.d)
+    do = step.dog.float().view(w.N * w.b, w.s, w.h_local, w.d)
+    sk = dk.sum(1)
+    norm_k = dk.square().sum(1).sqrt()
+    assert (sk.abs() <= 0.05 * norm_k + 1e-3).all(), "sum_j dK_j must vanish"
+    sv = dv.sum(1) - do.sum(1)
+    norm_v = dv.square().sum(1).sqrt()
+    assert (sv.abs() <= 0.05 * norm_v + 1e-3).all(), "sum_j dV_j must equal sum_i dO_i"
+
+
+def _check_tiny_split_q(w, ins):
+    """The tiny workload's second reading: Q split into two 64-row shards, each against
+    the full K/V prefix (q_offset = shard start), concatenated = unsharded attention."""
+    full = workloads.make_inputs(w, device="cuda")
+    # full-sequence [b][s][h][d] tensors, rebuilt from the shards by row order
+    q, k, v, do = (full[n].permute(1, 0, 2, 3, 4).reshape(w.b, w.s, w.h, w.d).contiguous()
+                   for n in ("q", "k", "v", "dout"))
+    o, lse, dq, dk, dv = _run(q, k, v, do, True)
+    half = w.s // w.split_q
+    outs, dks, dvs = [], torch.zeros_like(dk, dtype=torch.float32), torch.zeros_like(dv, dtype=torch.float32)
+    for r in range(w.split_q):
+        lo = r * half
+        so, sl, sdq, sdk, sdv = _run(q[:, lo:lo + half].contiguous(), k, v,
+                                     do[:, lo:lo + half].contiguous(), True, q_offset=lo)
+        outs.append(so)
+        dks += sdk.float()
+        dvs += sdv.float()
+    assert torch.equal(torch.cat(outs, 1).view(torch.int16), o.view(torch.int16))
+    orc = oracle.default()
+    rdq, rdk, rdv = orc.attn_bwd(f64(q), f64(k), f64(v), f64(do), True)
+    check_grad(dks.double().cpu().numpy(), rdk, "tiny split-Q dk sum")
+    check_grad(dvs.double().cpu().numpy(), rdv, "tiny split-Q dv sum")
+
+
+@pytest.mark.parametrize("name", ["llama70b", "ulysses131k"])
+def test_workload_sampled_rows(name):
+    """Long workloads: sampled query rows (out, lse, dq) and the last key rows (dk, dv)
+    of sampled heads against the oracle, plus the gradient-sum properties on every head."""
+    need_gpu()
+    w = workloads.WORKLOADS[name]
+    ins = workloads.make_inputs(w, device="cuda")
+    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal)
+    step.forward(ins["q"], ins["k"], ins["v"])
+    step.backward(ins["dout"])
+    torch.cuda.synchronize()
+    check_status()
+    # head->seq of the outputs is covered bit-exactly by the relayout tests; here the
+    # group-layout results are compared, and the shard outputs must be their regrouping
+    for g_t, s_t in ((step.og, step.o), (step.dqg, step.dq)):
+        again = sp_relayout_head2seq([g_t], w.N)[0]
+        assert torch.equal(again.view(torch.int16), s_t.view(torch.int16))
+    orc = oracle.default()
+    rows = [0, 1, 127, 128, w.s // 2 + 5, w.s - 129, w.s - 1]
+    keys = (w.s - 256, w.s)
+    for gi, j in ((0, 0), (w.N - 1, w.h_local - 1)):
+        tensors = [t[gi, 0, :, j, :].double().cpu().numpy()[None, :, None, :]
+                   for t in (step.qg, step.kg, step.vg, step.dog)]
+        tag = f"{name} group {gi} head {j}"
+        for i in rows:
+            ro, rl = orc.attn_fwd_rows(*tensors[:3], 0, 0, i, i + 1, True)
+            check_out(step.og[gi, 0, i, j].double().cpu().numpy()[None], ro, f"{tag} row {i} out")
+            assert abs(step.lse[gi * w.b, j, i].item() - rl[0]) <= 1e-2
+        dq_ref = []
+        dq_gpu = []
+        for i in rows:
+            rdq, _, _ = orc.attn_bwd_rows(*tensors, 0, 0, i, i + 1, 0, 0, True)
+            dq_ref.append(rdq)
+            dq_gpu.append(step.dqg[gi, 0, i, j].double().cpu().numpy()[None])
+        check_grad(np.concatenate(dq_gpu), np.concatenate(dq_ref), f"{tag} dq rows")
+        _, rdk, rdv = orc.attn_bwd_rows(*tensors, 0, 0, 0, 0, keys[0], keys[1], True)
+        check_grad(step.dkg[gi, 0, keys[0]:keys[1], j].double().cpu().numpy(), rdk, f"{tag} dk rows")
+        check_grad(step.dvg[gi, 0, keys[0]:keys[1], j].double().cpu().numpy(), rdv, f"{tag} dv rows")
+    _check_gradient_sums(step, w)
