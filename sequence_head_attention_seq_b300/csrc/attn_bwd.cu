@@ -11,18 +11,13 @@
 //      rows get lse = +inf, D = 0 so they contribute nothing), and zero the fp32
 //      dQ accumulator.  Bandwidth bound.
 //   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
-//      128-row query tiles that can see it (causal: from the diagonal down):
-//        warp 0      TMA producer (K, V once; Q_i, dO_i and row stats per tile, 2 stages)
-//        warp 1      MMA issuer and TMEM owner
-//        warps 4..7  P/dS computation (thread = one key row = one TMEM lane),
-//                    dQ drain, dK/dV epilogue
-//      TMEM (512 columns): [0,128) S^T then P^T (bf16, first half) and one dQ half,
-//      [128,256) dP^T then dS^T (bf16, first half) and the other dQ half,
-//      then dK and dV accumulators.
+//      128-row query tiles that can see it (causal: from the diagonal down).  Two
+//      compute warpgroups each own 64 of a tile's query columns, so the tensor core
+//      works on one half while the other half's P/dS is computed (see the kernel).
 //        S^T = K Q_i^T, dP^T = V dO_i^T        (A, B from shared memory, K-major)
-//        dV += P^T dO_i,  dK += dS^T Q_i       (A from TMEM, B MN-major in smem)
-//        dQ_i = dS K                           (dS written to smem by the P/dS
-//                                               warps, MN-major A; K MN-major B)
+//        dV += P^T dO_i                        (P^T from TMEM, dO MN-major in smem)
+//        dK += dS^T Q_i                        (dS^T K-major in smem, Q MN-major)
+//        dQ_i = dS K                           (the same dS tile read MN-major; K MN-major)
 //      dQ_i is added into the fp32 workspace with vector reductions.
 //   3. bwd_dq_convert: dq = bf16(scale * accumulator).  Bandwidth bound.
 #include "internal.h"
@@ -33,7 +28,7 @@ namespace {
 
 constexpr int kRows = 128;   // query rows per tile
 constexpr int kKeys = 128;   // keys per CTA
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- 1. row statistics
@@ -133,9 +128,10 @@ struct BwdSmem {
   alignas(1024) uint8_t v[kTileBytes];
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t dout[2][kTileBytes];
-  alignas(1024) uint8_t ds[kKeys * kRows * 2];    // dS as [key][query], 2 chunks of 64 queries
+  // dS as [key][query]: chunk h holds query columns [64h, 64h+64) of the tile
+  alignas(1024) uint8_t ds[kKeys * kRows * 2];
   alignas(16) float stats[2][2][kRows];            // [stage][lse2 | D][row]
-  uint64_t kv_full, q_full[2], q_empty[2], s_full, p_full, dq_full, dq_empty, dkv_full, drain;
+  uint64_t kv_full, q_full[2], q_empty[2], s_full[2], pds[2], dq_full, dq_empty, dkv_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -159,14 +155,30 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
   return n;
 }
 
+// Threads: warp 0 TMA, warp 1 MMA (+ TMEM), warps 4..7 and 8..11 = compute warpgroups
+// WG0 / WG1, each owning 64 of the 128 query columns of every tile.
+//
+// TMEM columns (128 lanes = the CTA's 128 keys):
+//   [0,64)    S^T for query half 0; P^T (bf16) is written over its first 32 columns
+//   [64,128)  S^T for query half 1; P^T over [64,96)
+//   [128,256) dP^T for halves 0 and 1; once both halves are read, dQ (lanes = queries)
+//   [256,256+D) dK accumulator, [256+D,256+2D) dV accumulator
+// Per query tile the MMA thread issues
+//   S^T_0, S^T_1 | (dQ of the previous tile drained) dP^T_0, dP^T_1 |
+//   dV += P^T_0 dO_0, dK += dS^T_0 Q_0 | dV += P^T_1 dO_1, dK += dS^T_1 Q_1 | dQ = dS K
+// so half 1's products run while WG0 works on half 0, and the next tile's S^T runs
+// while both warpgroups drain dQ.  The next tile's S^T overwrites the P^T columns only
+// after the dV products that read them were issued (tcgen05 MMAs of one thread run
+// in issue order).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdKernelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
   constexpr int kChunks = D / 64;
   constexpr uint32_t kTileBytes = BwdSmem<D>::kTileBytes;
-  constexpr uint32_t kColS = 0, kColDP = 128;
+  constexpr uint32_t kColDP = 128, kColDQ = 128;
   constexpr uint32_t kColDK = 256, kColDV = 256 + D;
+  constexpr int kHalf = kRows / 2;                 // query columns per warpgroup
 
   const AttnGeom& g = p.g;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -185,11 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.pds[s], kKeys);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, kKeys);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_empty, kKeys);
+    mbar_init(&sm.dq_empty, 2 * kKeys);
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
@@ -230,50 +242,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     }
   } else if (warp == 1 && lane == 0 && nq > 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_bf16(kKeys, kRows, false, false);   // M = keys, N = queries
+    constexpr uint32_t kIdS = idesc_bf16(kKeys, kHalf, false, false);   // [keys x 64 queries]
     constexpr uint32_t kIdKV = idesc_bf16(kKeys, D, false, true);       // dK, dV: N = d
-    constexpr uint32_t kIdQ = idesc_bf16(kRows, 64, true, true);        // dQ half: N = 64
+    constexpr uint32_t kIdQ = idesc_bf16(kRows, D, true, true);         // dQ: M = queries, N = d
     const uint32_t k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v), ds_addr = smem_u32(sm.ds);
     bool ok = mbar_wait(&sm.kv_full, 0, p.status, abort_flag);
     for (int it = 0; it < nq && ok; ++it) {
       const int s = it & 1;
       if (!(ok = mbar_wait(&sm.q_full[s], (it >> 1) & 1, p.status, abort_flag))) break;
-      if (it > 0 && !(ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abort_flag))) break;
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sm.q[s]), do_addr = smem_u32(sm.dout[s]);
-      // S^T = K Q^T and dP^T = V dO^T, contracting over d
+      // S^T halves: K [keys x d] times the 64 query rows of each half, contracting over d
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-        mma_ss(tmem + kColS, sdesc_sw128(k_addr + off, 16, 1024),
-               sdesc_sw128(q_addr + off, 16, 1024), kIdS, kk > 0);
-      }
+      for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-        mma_ss(tmem + kColDP, sdesc_sw128(v_addr + off, 16, 1024),
-               sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0);
-      }
-      mma_commit(&sm.s_full);
-      if (!(ok = mbar_wait(&sm.p_full, it & 1, p.status, abort_flag))) break;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss(tmem + hf * kHalf, sdesc_sw128(k_addr + off, 16, 1024),
+                 sdesc_sw128(q_addr + hf * 8192 + off, 16, 1024), kIdS, kk > 0);
+        }
+      // dP^T halves overwrite the previous tile's dQ: wait until it has been drained
+      if (it > 0 && !(ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abort_flag))) break;
       tc_fence_after();
-      // dV += P^T dO, dK += dS^T Q, contracting over the 128 query rows
 #pragma unroll
-      for (int kk = 0; kk < kRows / 16; ++kk) {
-        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-        mma_ts(tmem + kColDV, tmem + kColS + kk * 8,
-               sdesc_sw128(do_addr + kk * 2048, 16384, 1024), kIdKV, acc);
-        mma_ts(tmem + kColDK, tmem + kColDP + kk * 8,
-               sdesc_sw128(q_addr + kk * 2048, 16384, 1024), kIdKV, acc);
+      for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss(tmem + kColDP + hf * kHalf, sdesc_sw128(v_addr + off, 16, 1024),
+                 sdesc_sw128(do_addr + hf * 8192 + off, 16, 1024), kIdS, kk > 0);
+        }
+        mma_commit(&sm.s_full[hf]);
       }
-      // dQ = dS K, contracting over the 128 keys; N = d split in halves of 64
+      // dV += P^T dO and dK += dS^T Q, one query half at a time (K = 64 queries)
 #pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk) {
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!(ok = mbar_wait(&sm.pds[hf], it & 1, p.status, abort_flag))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int hf = 0; hf < kChunks; ++hf)
-          mma_ss(tmem + (hf == 0 ? 64u : 192u), sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
-                 sdesc_sw128(k_addr + hf * 16384 + kk * 2048, 16384, 1024), kIdQ, kk > 0);
+        for (int kk = 0; kk < kHalf / 16; ++kk) {
+          const uint32_t acc = (it > 0 || hf > 0 || kk > 0) ? 1u : 0u;
+          const uint32_t qrow = hf * 8192 + kk * 2048;      // 16 query rows
+          mma_ts(tmem + kColDV, tmem + hf * kHalf + kk * 8,
+                 sdesc_sw128(do_addr + qrow, 16384, 1024), kIdKV, acc);
+          mma_ss(tmem + kColDK, sdesc_sw128(ds_addr + hf * 16384 + kk * 32, 16, 1024),
+                 sdesc_sw128(q_addr + qrow, 16384, 1024), kIdKV, acc);
+        }
       }
+      if (!ok) break;
+      // dQ = dS K, contracting over the 128 keys: dS as an MN-major A (queries contiguous)
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk)
+        mma_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
+               sdesc_sw128(k_addr + kk * 2048, 16384, 1024), kIdQ, kk > 0);
       mma_commit(&sm.dq_full);
       mma_commit(&sm.q_empty[s]);
     }
@@ -285,33 +306,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ P / dS, dQ drain, epilogue
+    const int wg = (warp - 4) / 4;                   // query half owned by this warpgroup
     const int quad = warp % 4;
     const int jj = quad * 32 + lane;                 // key row in tile == TMEM lane
     const int key = kv0 + jj;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    uint8_t* ds_row = sm.ds + jj * 128;              // row jj of each 64-query chunk
+    const uint32_t s_col = wg * kHalf;
+    const uint32_t dp_col = kColDP + wg * kHalf;
+    uint8_t* ds_row = sm.ds + wg * 16384 + jj * 128; // row jj of this half's dS chunk
     const int swz = jj & 7;
+    const bool key_ok = key < kvlen;
     bool ok = true;
     for (int it = 0; it < nq; ++it) {
       const int s = it & 1;
       const int q0 = (m_start + it) * kRows;
       ok = mbar_wait(&sm.q_full[s], (it >> 1) & 1, p.status, abort_flag);
-      ok = ok && mbar_wait(&sm.s_full, it & 1, p.status, abort_flag);
+      ok = ok && mbar_wait(&sm.s_full[wg], it & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = sm.stats[s][0];
-      const float* Dv = sm.stats[s][1];
+      const float* lse2 = sm.stats[s][0] + wg * kHalf;
+      const float* Dv = sm.stats[s][1] + wg * kHalf;
+      const int qh0 = q0 + wg * kHalf;               // first query row of this half
       const bool need_mask = (kv0 + kKeys > kvlen) ||
-                             (g.causal && kv0 + kKeys - 1 > g.q_offset + q0);
-      // first query row that sees this key (causal), relative to q0
-      const int first_q = g.causal ? key - g.q_offset - q0 : -(1 << 30);
-      const bool key_ok = key < kvlen;
+                             (g.causal && kv0 + kKeys - 1 > g.q_offset + qh0);
+      // first query column (relative to the half) that sees this key under the causal mask
+      const int first_q = g.causal ? key - g.q_offset - qh0 : -(1 << 30);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kRows; c0 += 32) {
+      for (int c0 = 0; c0 < kHalf; c0 += 32) {
         uint32_t sraw[32], draw[32];
-        tmem_ld32(lane_base + kColS + c0, sraw);
-        tmem_ld32(lane_base + kColDP + c0, draw);
+        tmem_ld32(lane_base + s_col + c0, sraw);
+        tmem_ld32(lane_base + dp_col + c0, draw);
         tmem_ld_wait();
         uint32_t pk[16], dk2[16];
 #pragma unroll
@@ -328,44 +353,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           pk[i] = pack_bf16x2(pv[0], pv[1]);
           dk2[i] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        tmem_st16(lane_base + kColS + c0 / 2, pk);
-        tmem_st16(lane_base + kColDP + c0 / 2, dk2);
-        // dS row into the swizzled [key][query] tile: 4 x 16-byte units
-        const int chunk = c0 / 64;
-        const int u0 = (c0 % 64) / 8;
+        tmem_st16(lane_base + s_col + c0 / 2, pk);
+        // dS row into the swizzled [key][query] chunk of this half: 4 x 16-byte units
+        const int u0 = c0 / 8;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          uint4* dst = reinterpret_cast<uint4*>(ds_row + chunk * 16384 + (((u0 + u) ^ swz) * 16));
+          uint4* dst = reinterpret_cast<uint4*>(ds_row + (((u0 + u) ^ swz) * 16));
           *dst = make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
         }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm.p_full);
-      // dQ_i = dS K is ready: lane jj now holds query row q0 + jj
+      mbar_arrive(&sm.pds[wg]);
+      // dQ = dS K is ready: lane jj now holds query row q0 + jj; this warpgroup drains
+      // its half of the d columns
       ok = mbar_wait(&sm.dq_full, it & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float* dst = p.dq_acc + (static_cast<int64_t>(bh) * p.rows + q0 + jj) * D;
+      float* dst = p.dq_acc + (static_cast<int64_t>(bh) * p.rows + q0 + jj) * D + wg * (D / 2);
 #pragma unroll
-      for (int hf = 0; hf < kChunks; ++hf) {
+      for (int c = 0; c < D / 2; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + kColDQ + wg * (D / 2) + c, r);
+        tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + (hf == 0 ? 64u : 192u) + c, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(dst + hf * 64 + c + e, __uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                       __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-        }
+        for (int e = 0; e < 32; e += 4)
+          red_add_v4(dst + c + e, __uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                     __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
       }
       tc_fence_before();
       mbar_arrive(&sm.dq_empty);
     }
-    // epilogue: dK = scale * acc, dV = acc (zero when no query row sees this key block)
+    // epilogue: dK = scale * acc, dV = acc (zero when no query row sees this key block);
+    // each warpgroup writes its half of the d columns
     const bool have = nq > 0;
     if (have && ok) {
       ok = mbar_wait(&sm.dkv_full, 0, p.status, abort_flag);
@@ -374,16 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     }
     const bool store = key < g.sk;
     __nv_bfloat16* dk_row = p.dk + b * p.k_stride[0] + static_cast<int64_t>(key) * p.k_stride[1] +
-                            h * p.k_stride[2];
+                            h * p.k_stride[2] + wg * (D / 2);
     __nv_bfloat16* dv_row = p.dv + b * p.v_stride[0] + static_cast<int64_t>(key) * p.v_stride[1] +
-                            h * p.v_stride[2];
+                            h * p.v_stride[2] + wg * (D / 2);
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
-      const uint32_t col = which == 0 ? kColDK : kColDV;
+      const uint32_t col = (which == 0 ? kColDK : kColDV) + wg * (D / 2);
       const float mul = which == 0 ? g.scale : 1.0f;
       __nv_bfloat16* row = which == 0 ? dk_row : dv_row;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < D / 2; c += 32) {
         uint32_t r[32];
         if (have && ok) {
           tmem_ld32(lane_base + col + c, r);
@@ -397,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-          uint4* dst = reinterpret_cast<uint4*>(row + c);
+          uint4* o = reinterpret_cast<uint4*>(row + c);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            o[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       }
     }
