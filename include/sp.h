@@ -142,6 +142,31 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse,
                       const void* dout, void* dq, void* dk, void* dv, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch array that sp_attn_bwd_noalloc uses (32 MiB). */
+#define SP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * sp_attn_bwd for callers that cannot allocate device memory: code running inside a
+ * framework or runtime that owns all device memory (no cudaMalloc/cudaFree allowed on
+ * its threads), or code bound to a fixed memory plan.  The paper has no counterpart.
+ *
+ * Instead of a caller-supplied workspace it uses a library-owned device array of
+ * SP_NOALLOC_SCRATCH_BYTES, created on every GPU that loads the library and kept
+ * until the process exits.  It never calls cudaMalloc, cudaFree or any allocating
+ * routine.  Arguments, outputs and results are those of sp_attn_bwd.
+ *
+ *  - Problems whose workspace (sp_attn_bwd_workspace_size) exceeds
+ *    SP_NOALLOC_SCRATCH_BYTES are rejected with SP_ERR_WORKSPACE before any launch.
+ *  - The first call on each device looks up the array's device address (with that
+ *    device current); make that first call before capturing any stream.
+ *  - All calls share the one array per device and it keeps whatever the last call
+ *    left in it (every byte is rewritten before it is read, so nothing needs
+ *    clearing).  Calls whose kernels overlap on the GPU (different streams without
+ *    ordering between them) race on it: serialise them.
+ */
+sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, void* stream);
+
 /*
  * Synchronises `stream`, then reads and clears the device status word that the
  * kernels set when a bounded device-side wait gives up (SP_ERR_TIMEOUT) or a

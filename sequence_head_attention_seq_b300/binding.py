@@ -28,8 +28,9 @@ MAX_RELAYOUT_TENSORS = 8
 
 # Every symbol include/sp.h declares.
 EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_attn_fwd",
-           "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_get_device_status",
-           "sp_status_string"]
+           "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_bwd_noalloc",
+           "sp_get_device_status", "sp_status_string"]
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # SP_NOALLOC_SCRATCH_BYTES
 
 
 class SpError(RuntimeError):
@@ -83,6 +84,8 @@ def load(build_if_missing: bool = True):
         lib.sp_attn_bwd_workspace_size.restype = ctypes.c_size_t
         lib.sp_attn_bwd.argtypes = [pp] + [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p]
         lib.sp_attn_bwd.restype = i
+        lib.sp_attn_bwd_noalloc.argtypes = [pp] + [ctypes.c_void_p] * 7
+        lib.sp_attn_bwd_noalloc.restype = i
         lib.sp_get_device_status.argtypes = [ctypes.c_void_p]
         lib.sp_get_device_status.restype = i
         lib.sp_status_string.argtypes = [i]
@@ -250,6 +253,40 @@ def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                          workspace.numel() * workspace.element_size(), _stream(q.device))
     _check("sp_attn_bwd", rc)
+    return dq, dk, dv
+
+
+def sp_attn_bwd_noalloc(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
+                        key_len=None, softmax_scale=None, dq=None, dk=None, dv=None):
+    """sp_attn_bwd with the library's own fixed device scratch instead of a workspace.
+
+    For callers that must not allocate device memory during the call: the C entry
+    point allocates nothing (pass preallocated dq/dk/dv to keep this wrapper from
+    allocating them either).  Problems needing more than NOALLOC_SCRATCH_BYTES of
+    workspace raise SpError(SP_ERR_WORKSPACE); concurrent calls on unordered
+    streams share the scratch and must not overlap.
+    """
+    lib = load()
+    _need_bf16_cuda("out", out)
+    _need_bf16_cuda("dout", dout)
+    if out.shape != dout.shape or not _same_layout(out, dout):
+        raise ValueError("out and dout must share shape and strides")
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale)
+
+    def like(t):
+        return torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=t.device)
+
+    dq = like(q) if dq is None else dq
+    dk = like(k) if dk is None else dk
+    dv = like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _need_bf16_cuda(name, t)
+        if t.shape != ref.shape or not _same_layout(t, ref):
+            raise ValueError(f"{name} must have the shape and strides of its input")
+    rc = lib.sp_attn_bwd_noalloc(ctypes.byref(p), out.data_ptr(), lse.data_ptr(),
+                                 dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                 _stream(q.device))
+    _check("sp_attn_bwd_noalloc", rc)
     return dq, dk, dv
 
 
