@@ -182,8 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 
   const AttnGeom& g = p.g;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.x % (g.B * g.H);
-  const int n = blockIdx.x / (g.B * g.H);          // key tile; small n = most work (causal)
+  // key tiles of one (batch entry, head) are consecutive so that its Q, dO and dQ
+  // accumulator stay in L2 while they run; small n = most work (causal) goes first
+  const int bh = blockIdx.x / p.num_kv_tiles;
+  const int n = blockIdx.x % p.num_kv_tiles;
   const int b = bh / g.H, h = bh % g.H;
   const int kv0 = n * kKeys;
   const int kvlen = kv_limit(g, b);

@@ -85,8 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   const AttnGeom& g = p.g;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.x % (g.B * g.H);
-  const int pair = p.num_pairs - 1 - blockIdx.x / (g.B * g.H);   // heavy (late) tiles first
+  // tiles of one (batch entry, head) are consecutive so that its K/V stay in L2 while
+  // they run; within a head the heavy (late, causal) tiles go first
+  const int bh = blockIdx.x / p.num_pairs;
+  const int pair = p.num_pairs - 1 - blockIdx.x % p.num_pairs;
   const int b = bh / g.H, h = bh % g.H;
   const int kvlen = kv_limit(g, b);
   const TileInfo ti[2] = {tile_info(g, kvlen, pair * 2 * kRows),
