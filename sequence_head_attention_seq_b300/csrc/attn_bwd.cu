@@ -13,12 +13,16 @@
 //   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
 //      128-row query tiles that can see it (causal: from the diagonal down).  Two
 //      compute warpgroups each own 64 of a tile's query columns, so the tensor core
-//      works on one half while the other half's P/dS is computed (see the kernel).
-//        S^T = K Q_i^T, dP^T = V dO_i^T        (A, B from shared memory, K-major)
+//      works on one half's dV/dK while the other half's P/dS is computed.
+//        S^T = K Q_i^T, dP^T = V dO_i^T        (A, B from shared memory, K-major;
+//                                               N = 128: an N = 64 product takes
+//                                               as long as an N = 128 one)
 //        dV += P^T dO_i                        (P^T from TMEM, dO MN-major in smem)
 //        dK += dS^T Q_i                        (dS^T K-major in smem, Q MN-major)
 //        dQ_i = dS K                           (the same dS tile read MN-major; K MN-major)
-//      dQ_i is added into the fp32 workspace with vector reductions.
+//      dQ_i is read out of TMEM at once (so the next tile's dP^T can reuse the
+//      columns), staged in the warp's own slice of the dS tile and added into the
+//      fp32 workspace by TMA tensor reduce-adds.
 //   3. bwd_dq_convert: dq = bf16(scale * accumulator).  Bandwidth bound.
 #include "internal.h"
 #include "ptx.cuh"
@@ -131,13 +135,14 @@ struct BwdSmem {
   // dS as [key][query]: chunk h holds query columns [64h, 64h+64) of the tile
   alignas(1024) uint8_t ds[kKeys * kRows * 2];
   alignas(16) float stats[2][2][kRows];            // [stage][lse2 | D][row]
-  uint64_t kv_full, q_full[2], q_empty[2], s_full[2], pds[2], dq_full, dq_empty, dkv_full, drain;
+  uint64_t kv_full, q_full[2], q_empty[2], s_full, pds[2], dq_full, dq_empty, dkv_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct BwdKernelParams {
   CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tdq;        // fp32 dQ accumulator as [B*H*rows][D], 32 x 32 boxes
   const float* stats;     // [B][H][2][rows]
   float* dq_acc;          // [B][H][rows][D]
   __nv_bfloat16* dk;
@@ -161,15 +166,21 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
 // TMEM columns (128 lanes = the CTA's 128 keys):
 //   [0,64)    S^T for query half 0; P^T (bf16) is written over its first 32 columns
 //   [64,128)  S^T for query half 1; P^T over [64,96)
-//   [128,256) dP^T for halves 0 and 1; once both halves are read, dQ (lanes = queries)
+//   [128,256) dP^T; once both halves are read, dQ (lanes = queries)
 //   [256,256+D) dK accumulator, [256+D,256+2D) dV accumulator
 // Per query tile the MMA thread issues
-//   S^T_0, S^T_1 | (dQ of the previous tile drained) dP^T_0, dP^T_1 |
+//   S^T | (dQ of the previous tile read out) dP^T |
 //   dV += P^T_0 dO_0, dK += dS^T_0 Q_0 | dV += P^T_1 dO_1, dK += dS^T_1 Q_1 | dQ = dS K
-// so half 1's products run while WG0 works on half 0, and the next tile's S^T runs
-// while both warpgroups drain dQ.  The next tile's S^T overwrites the P^T columns only
-// after the dV products that read them were issued (tcgen05 MMAs of one thread run
+// so half 1's P/dS is computed while half 0's products run, and the next tile's S^T
+// runs while the warpgroups read dQ out.  The next tile's S^T overwrites the P^T
+// columns only after the dV products that read them (tcgen05 MMAs of one thread run
 // in issue order).
+//
+// dQ leaves through shared memory: after the dQ product completes, the dS tile has no
+// reader left, so each compute warp stages its 32 query rows x 32-column boxes of dQ
+// in its own 4 KB slice of that tile (the slice it writes dS into) and one lane issues
+// a TMA reduce-add of the box into the accumulator.  The warp waits for TMA to finish
+// reading the slice before it writes the next box or the next tile's dS there.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdKernelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -199,9 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
-      mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.pds[s], kKeys);
     }
+    mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_empty, 2 * kKeys);
     mbar_init(&sm.dkv_full, 1);
@@ -224,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tma_prefetch_desc(&p.tk);
     tma_prefetch_desc(&p.tv);
     tma_prefetch_desc(&p.tdo);
+    tma_prefetch_desc(&p.tdq);
     mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
     for (int c = 0; c < kChunks; ++c) {
       tma_load_4d(sm.k + c * 16384, &p.tk, &sm.kv_full, c * 64, h, kv0, b);
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     }
   } else if (warp == 1 && lane == 0 && nq > 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_bf16(kKeys, kHalf, false, false);   // [keys x 64 queries]
+    constexpr uint32_t kIdS = idesc_bf16(kKeys, kRows, false, false);   // [keys x queries]
     constexpr uint32_t kIdKV = idesc_bf16(kKeys, D, false, true);       // dK, dV: N = d
     constexpr uint32_t kIdQ = idesc_bf16(kRows, D, true, true);         // dQ: M = queries, N = d
     const uint32_t k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v), ds_addr = smem_u32(sm.ds);
@@ -254,28 +266,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       if (!(ok = mbar_wait(&sm.q_full[s], (it >> 1) & 1, p.status, abort_flag))) break;
       tc_fence_after();
       const uint32_t q_addr = smem_u32(sm.q[s]), do_addr = smem_u32(sm.dout[s]);
-      // S^T halves: K [keys x d] times the 64 query rows of each half, contracting over d
+      // S^T = K Q^T: K [keys x d] times the tile's 128 query rows, contracting over d
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + hf * kHalf, sdesc_sw128(k_addr + off, 16, 1024),
-                 sdesc_sw128(q_addr + hf * 8192 + off, 16, 1024), kIdS, kk > 0);
-        }
-      // dP^T halves overwrite the previous tile's dQ: wait until it has been drained
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+        mma_ss(tmem, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
+               kIdS, kk > 0);
+      }
+      // dP^T overwrites the previous tile's dQ: wait until it has been read out of TMEM
       if (it > 0 && !(ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abort_flag))) break;
       tc_fence_after();
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + kColDP + hf * kHalf, sdesc_sw128(v_addr + off, 16, 1024),
-                 sdesc_sw128(do_addr + hf * 8192 + off, 16, 1024), kIdS, kk > 0);
-        }
-        mma_commit(&sm.s_full[hf]);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+        mma_ss(tmem + kColDP, sdesc_sw128(v_addr + off, 16, 1024),
+               sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0);
       }
+      mma_commit(&sm.s_full);
       // dV += P^T dO and dK += dS^T Q, one query half at a time (K = 64 queries)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
@@ -323,10 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const int s = it & 1;
       const int q0 = (m_start + it) * kRows;
       ok = mbar_wait(&sm.q_full[s], (it >> 1) & 1, p.status, abort_flag);
-      ok = ok && mbar_wait(&sm.s_full[wg], it & 1, p.status, abort_flag);
+      ok = ok && mbar_wait(&sm.s_full, it & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      // this warp's slice of the dS tile held the previous tile's last dQ box
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
       const float* lse2 = sm.stats[s][0] + wg * kHalf;
       const float* Dv = sm.stats[s][1] + wg * kHalf;
       const int qh0 = q0 + wg * kHalf;               // first query row of this half
@@ -368,26 +378,45 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.pds[wg]);
-      // dQ = dS K is ready: lane jj now holds query row q0 + jj; this warpgroup drains
-      // its half of the d columns
+      // dQ = dS K is ready: lane jj now holds query row q0 + jj; this warpgroup takes
+      // its half of the d columns out of TMEM, then releases the columns
       ok = mbar_wait(&sm.dq_full, it & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float* dst = p.dq_acc + (static_cast<int64_t>(bh) * p.rows + q0 + jj) * D + wg * (D / 2);
+      constexpr int kBoxes = D / 64;                 // 32-column boxes per warpgroup half
+      uint32_t r[kBoxes][32];
 #pragma unroll
-      for (int c = 0; c < D / 2; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + kColDQ + wg * (D / 2) + c, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          red_add_v4(dst + c + e, __uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                     __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-      }
+      for (int bx = 0; bx < kBoxes; ++bx) tmem_ld32(lane_base + kColDQ + wg * (D / 2) + bx * 32, r[bx]);
+      tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&sm.dq_empty);
+      // stage each box (this warp's 32 rows x 32 columns, 128-byte swizzle) in the warp's
+      // slice of the dS tile, which the completed dQ product no longer reads
+      uint8_t* stage = sm.ds + wg * 16384 + quad * 4096;
+      uint8_t* srow = stage + lane * 128;
+      const int acc_row = static_cast<int>(static_cast<int64_t>(bh) * p.rows) + q0 + quad * 32;
+#pragma unroll
+      for (int bx = 0; bx < kBoxes; ++bx) {
+        if (bx > 0) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) * 16)) =
+              make_uint4(r[bx][4 * u], r[bx][4 * u + 1], r[bx][4 * u + 2], r[bx][4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&p.tdq, stage, wg * (D / 2) + bx * 32, acc_row);
+          bulk_commit();
+        }
+      }
     }
+    // the accumulator adds must be complete (and the slice read) before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     // epilogue: dK = scale * acc, dV = acc (zero when no query row sees this key block);
     // each warpgroup writes its half of the d columns
     const bool have = nq > 0;
@@ -471,6 +500,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     p.tk = a.tk;
     p.tv = a.tv;
     p.tdo = a.tdo;
+    p.tdq = a.tdq;
     p.stats = a.row_stats;
     p.dq_acc = a.dq_acc;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);

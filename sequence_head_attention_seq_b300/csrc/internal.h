@@ -31,6 +31,10 @@ inline int64_t padded_rows(int sq) { return (static_cast<int64_t>(sq) + 127) / 1
 bool encode_rows_map(CUtensorMap* map, const void* base, int d, int S, int H, int B,
                      const int64_t stride[3]);
 
+// 2-D TMA map over the fp32 dQ accumulator viewed as [rows_total][d], box = 32
+// columns x 32 rows, 128-byte swizzle (the backward reduces dQ tiles into it).
+bool encode_acc_map(CUtensorMap* map, const float* base, int d, int64_t rows_total);
+
 struct FwdArgs {
   CUtensorMap tq, tk, tv;
   void* o;
@@ -43,6 +47,7 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tdq;     // over dq_acc (encode_acc_map)
   const void* o;
   const void* dout;
   int64_t o_stride[3];

@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -148,6 +149,20 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int d, int S, int H, in
   return r == CUDA_SUCCESS;
 }
 
+bool encode_acc_map(CUtensorMap* map, const float* base, int d, int64_t rows_total) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows_total)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t elem[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace sp
 
 using namespace sp;
@@ -205,6 +220,8 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
     return SP_ERR_MISALIGNED;
   if (g.B == 0 || g.H == 0) return SP_OK;
   const WorkspaceLayout w = workspace_layout(g);
+  // the dQ accumulator is addressed by 32-bit TMA row coordinates
+  if (static_cast<int64_t>(g.B) * g.H * padded_rows(g.sq) > INT32_MAX) return SP_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < w.total) return SP_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SP_ERR_MISALIGNED;
   BwdArgs a;
@@ -229,6 +246,10 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
   a.dv = dv;
   a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.dq_off);
   a.row_stats = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.stats_off);
+  if (g.sq > 0 && g.sk > 0 &&
+      !encode_acc_map(&a.tdq, a.dq_acc, g.d,
+                      static_cast<int64_t>(g.B) * g.H * padded_rows(g.sq)))
+    return SP_ERR_CUDA;
   a.g = g;
   a.status = status_word();
   if (a.status == nullptr) return SP_ERR_CUDA;
