@@ -19,10 +19,13 @@
 //                                               as long as an N = 128 one)
 //        dV += P^T dO_i                        (P^T from TMEM, dO MN-major in smem)
 //        dK += dS^T Q_i                        (dS^T K-major in smem, Q MN-major)
-//        dQ_i = dS K                           (the same dS tile read MN-major; K MN-major)
+//        dQ_i^T = K^T dS^T  (d = 128)          (K and the dS tile, both read MN-major)
+//        dQ_i   = dS K      (d = 64)
 //      dQ_i is read out of TMEM at once (so the next tile's dP^T can reuse the
-//      columns), staged in the warp's own slice of the dS tile and added into the
-//      fp32 workspace by TMA tensor reduce-adds.
+//      columns) and added into the fp32 workspace: for d = 128 straight from
+//      registers (TMEM lanes are head-dim indices, so a warp's 32 lanes add one
+//      contiguous 128-byte piece of a dQ row); for d = 64 staged in the warp's own
+//      slice of the dS tile and added by TMA tensor reduce-adds.
 //   3. bwd_dq_convert: dq = bf16(scale * accumulator).  Bandwidth bound.
 #include "internal.h"
 #include "ptx.cuh"
@@ -135,7 +138,8 @@ struct BwdSmem {
   // dS as [key][query]: chunk h holds query columns [64h, 64h+64) of the tile
   alignas(1024) uint8_t ds[kKeys * kRows * 2];
   alignas(16) float stats[2][2][kRows];            // [stage][lse2 | D][row]
-  uint64_t kv_full, q_full[2], q_empty[2], s_full, pds[2], dq_full, dq_empty, dkv_full, drain;
+  uint64_t kv_full, q_full[2], q_empty[2], s_full, s_read, pds[2], dq_full, dq_empty, dkv_full,
+      drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -164,23 +168,24 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
 // WG0 / WG1, each owning 64 of the 128 query columns of every tile.
 //
 // TMEM columns (128 lanes = the CTA's 128 keys):
-//   [0,64)    S^T for query half 0; P^T (bf16) is written over its first 32 columns
-//   [64,128)  S^T for query half 1; P^T over [64,96)
-//   [128,256) dP^T; once both halves are read, dQ (lanes = queries)
+//   [0,128)   S^T (query half h in [64h, 64h+64))
+//   [128,256) dP^T; each warpgroup writes its P^T (bf16) over the first 32 columns of
+//             the dP^T half it has read; after the dV products, dQ^T (d = 128: lanes =
+//             head-dim indices, columns = queries) or dQ (d = 64: lanes = queries)
 //   [256,256+D) dK accumulator, [256+D,256+2D) dV accumulator
-// Per query tile the MMA thread issues
-//   S^T | (dQ of the previous tile read out) dP^T |
-//   dV += P^T_0 dO_0, dK += dS^T_0 Q_0 | dV += P^T_1 dO_1, dK += dS^T_1 Q_1 | dQ = dS K
-// so half 1's P/dS is computed while half 0's products run, and the next tile's S^T
-// runs while the warpgroups read dQ out.  The next tile's S^T overwrites the P^T
-// columns only after the dV products that read them (tcgen05 MMAs of one thread run
-// in issue order).
+// Per query tile i the MMA thread issues
+//   (dQ_{i-1} read out) dP^T_i | (S^T_i read out) S^T_{i+1} |
+//   dV += P^T_0 dO_0, dK += dS^T_0 Q_0 | dV += P^T_1 dO_1, dK += dS^T_1 Q_1 | dQ_i = dS K
+// so the next tile's S^T runs while the warpgroups compute P and dS, half 1's P/dS is
+// computed while half 0's products run, and dQ_i's columns are released as soon as
+// the warpgroups have loaded them.  dQ_i overwrites the P^T columns only after the dV
+// products that read them (tcgen05 MMAs of one thread run in issue order).
 //
-// dQ leaves through shared memory: after the dQ product completes, the dS tile has no
-// reader left, so each compute warp stages its 32 query rows x 32-column boxes of dQ
+// d = 64: dQ leaves through shared memory.  After the dQ product completes, the dS tile
+// has no reader left, so each compute warp stages its 32 query rows x 32 columns of dQ
 // in its own 4 KB slice of that tile (the slice it writes dS into) and one lane issues
 // a TMA reduce-add of the box into the accumulator.  The warp waits for TMA to finish
-// reading the slice before it writes the next box or the next tile's dS there.
+// reading the slice before it writes the next tile's dS there.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdKernelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_init(&sm.pds[s], kKeys);
     }
     mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_read, 2 * kKeys);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_empty, 2 * kKeys);
     mbar_init(&sm.dkv_full, 1);
@@ -259,20 +265,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     constexpr uint32_t kIdS = idesc_bf16(kKeys, kRows, false, false);   // [keys x queries]
     constexpr uint32_t kIdKV = idesc_bf16(kKeys, D, false, true);       // dK, dV: N = d
     constexpr uint32_t kIdQ = idesc_bf16(kRows, D, true, true);         // dQ: M = queries, N = d
+    constexpr uint32_t kIdQT = idesc_bf16(D, kRows, true, true);        // dQ^T: M = d, N = queries
     const uint32_t k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v), ds_addr = smem_u32(sm.ds);
-    bool ok = mbar_wait(&sm.kv_full, 0, p.status, abort_flag);
-    for (int it = 0; it < nq && ok; ++it) {
-      const int s = it & 1;
-      if (!(ok = mbar_wait(&sm.q_full[s], (it >> 1) & 1, p.status, abort_flag))) break;
-      tc_fence_after();
-      const uint32_t q_addr = smem_u32(sm.q[s]), do_addr = smem_u32(sm.dout[s]);
-      // S^T = K Q^T: K [keys x d] times the tile's 128 query rows, contracting over d
+    // S^T = K Q^T: K [keys x d] times a tile's 128 query rows, contracting over d
+    auto issue_s = [&](uint32_t q_addr) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
         mma_ss(tmem, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
                kIdS, kk > 0);
       }
+    };
+    bool ok = mbar_wait(&sm.kv_full, 0, p.status, abort_flag);
+    ok = ok && mbar_wait(&sm.q_full[0], 0, p.status, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      issue_s(smem_u32(sm.q[0]));
+    }
+    for (int it = 0; it < nq && ok; ++it) {
+      const int s = it & 1;
+      const uint32_t q_addr = smem_u32(sm.q[s]), do_addr = smem_u32(sm.dout[s]);
       // dP^T overwrites the previous tile's dQ: wait until it has been read out of TMEM
       if (it > 0 && !(ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abort_flag))) break;
       tc_fence_after();
@@ -283,6 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0);
       }
       mma_commit(&sm.s_full);
+      // the next tile's S^T, as soon as this tile's S^T is in the warpgroups' registers
+      if (it + 1 < nq) {
+        if (!(ok = mbar_wait(&sm.s_read, it & 1, p.status, abort_flag))) break;
+        if (!(ok = mbar_wait(&sm.q_full[s ^ 1], ((it + 1) >> 1) & 1, p.status, abort_flag))) break;
+        tc_fence_after();
+        issue_s(smem_u32(sm.q[s ^ 1]));
+      }
       // dV += P^T dO and dK += dS^T Q, one query half at a time (K = 64 queries)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
@@ -292,20 +311,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         for (int kk = 0; kk < kHalf / 16; ++kk) {
           const uint32_t acc = (it > 0 || hf > 0 || kk > 0) ? 1u : 0u;
           const uint32_t qrow = hf * 8192 + kk * 2048;      // 16 query rows
-          mma_ts(tmem + kColDV, tmem + hf * kHalf + kk * 8,
+          mma_ts(tmem + kColDV, tmem + kColDP + hf * kHalf + kk * 8,
                  sdesc_sw128(do_addr + qrow, 16384, 1024), kIdKV, acc);
           mma_ss(tmem + kColDK, sdesc_sw128(ds_addr + hf * 16384 + kk * 32, 16, 1024),
                  sdesc_sw128(q_addr + qrow, 16384, 1024), kIdKV, acc);
         }
       }
       if (!ok) break;
-      // dQ = dS K, contracting over the 128 keys: dS as an MN-major A (queries contiguous)
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk)
-        mma_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
-               sdesc_sw128(k_addr + kk * 2048, 16384, 1024), kIdQ, kk > 0);
-      mma_commit(&sm.dq_full);
+      // Q_i and dO_i have no reader left: release the stage for tile i + 2's loads
       mma_commit(&sm.q_empty[s]);
+      // contracting over the 128 keys; K and the dS tile are both read MN-major
+      if constexpr (D == 128) {
+        // dQ^T = K^T dS^T: A = K^T (head-dim contiguous), B = dS^T (queries contiguous)
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          mma_ss(tmem + kColDQ, sdesc_sw128(k_addr + kk * 2048, 16384, 1024),
+                 sdesc_sw128(ds_addr + kk * 2048, 16384, 1024), kIdQT, kk > 0);
+      } else {
+        // dQ = dS K: A = dS (queries contiguous), B = K (head-dim contiguous)
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          mma_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
+                 sdesc_sw128(k_addr + kk * 2048, 16384, 1024), kIdQ, kk > 0);
+      }
+      mma_commit(&sm.dq_full);
     }
     mma_commit(&sm.dkv_full);
     if (!ok) {
@@ -334,9 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // this warp's slice of the dS tile held the previous tile's last dQ box
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
+      if constexpr (D == 64) {
+        // this warp's slice of the dS tile held the previous tile's dQ box
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
       const float* lse2 = sm.stats[s][0] + wg * kHalf;
       const float* Dv = sm.stats[s][1] + wg * kHalf;
       const int qh0 = q0 + wg * kHalf;               // first query row of this half
@@ -350,6 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tmem_ld32(lane_base + s_col + c0, sraw);
         tmem_ld32(lane_base + dp_col + c0, draw);
         tmem_ld_wait();
+        if (c0 + 32 == kHalf) {
+          // all of S^T is in registers: the next tile's S^T may overwrite it
+          tc_fence_before();
+          mbar_arrive(&sm.s_read);
+        }
         uint32_t pk[16], dk2[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -365,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           pk[i] = pack_bf16x2(pv[0], pv[1]);
           dk2[i] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        tmem_st16(lane_base + s_col + c0 / 2, pk);
+        tmem_st16(lane_base + dp_col + c0 / 2, pk);   // over dP^T columns already read
         // dS row into the swizzled [key][query] chunk of this half: 4 x 16-byte units
         const int u0 = c0 / 8;
 #pragma unroll
@@ -378,38 +414,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.pds[wg]);
-      // dQ = dS K is ready: lane jj now holds query row q0 + jj; this warpgroup takes
-      // its half of the d columns out of TMEM, then releases the columns
       ok = mbar_wait(&sm.dq_full, it & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      constexpr int kBoxes = D / 64;                 // 32-column boxes per warpgroup half
-      uint32_t r[kBoxes][32];
+      if constexpr (D == 128) {
+        // dQ^T is ready: lane jj holds head-dim index jj; this warpgroup takes its 64 query
+        // columns out of TMEM, releases them, then adds them row by row (a warp's lanes
+        // cover 32 consecutive head-dim entries of one query row: one 128-byte piece)
+        uint32_t r[2][32];
+        tmem_ld32(lane_base + kColDQ + wg * kHalf, r[0]);
+        tmem_ld32(lane_base + kColDQ + wg * kHalf + 32, r[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        float* dst = p.dq_acc + (static_cast<int64_t>(bh) * p.rows + q0 + wg * kHalf) * D + jj;
 #pragma unroll
-      for (int bx = 0; bx < kBoxes; ++bx) tmem_ld32(lane_base + kColDQ + wg * (D / 2) + bx * 32, r[bx]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&sm.dq_empty);
-      // stage each box (this warp's 32 rows x 32 columns, 128-byte swizzle) in the warp's
-      // slice of the dS tile, which the completed dQ product no longer reads
-      uint8_t* stage = sm.ds + wg * 16384 + quad * 4096;
-      uint8_t* srow = stage + lane * 128;
-      const int acc_row = static_cast<int>(static_cast<int64_t>(bh) * p.rows) + q0 + quad * 32;
+        for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-      for (int bx = 0; bx < kBoxes; ++bx) {
-        if (bx > 0) {
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-        }
+          for (int i = 0; i < 32; ++i) red_add(dst + (h2 * 32 + i) * D, __uint_as_float(r[h2][i]));
+      } else {
+        // dQ is ready: lane jj holds query row q0 + jj; this warpgroup takes its 32 of the
+        // 64 head-dim columns out of TMEM and releases them
+        uint32_t r[32];
+        tmem_ld32(lane_base + kColDQ + wg * 32, r);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        // stage the warp's 32 rows x 32 columns (128-byte swizzle) in its slice of the
+        // dS tile, which the completed dQ product no longer reads, and reduce it with TMA
+        uint8_t* stage = sm.ds + wg * 16384 + quad * 4096;
+        uint8_t* srow = stage + lane * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) * 16)) =
-              make_uint4(r[bx][4 * u], r[bx][4 * u + 1], r[bx][4 * u + 2], r[bx][4 * u + 3]);
+              make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_2d(&p.tdq, stage, wg * (D / 2) + bx * 32, acc_row);
+          tma_reduce_add_2d(&p.tdq, stage, wg * 32,
+                            static_cast<int>(static_cast<int64_t>(bh) * p.rows) + q0 + quad * 32);
           bulk_commit();
         }
       }
