@@ -12,8 +12,7 @@
 //      dQ accumulator.  Bandwidth bound.
 //   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
 //      128-row query tiles that can see it (causal: from the diagonal down).  Two
-//      compute warpgroups each own 64 of a tile's query columns, so the tensor core
-//      works on one half's dV/dK while the other half's P/dS is computed.
+//      compute warpgroups each own 64 of a tile's query columns.
 //        S^T = K Q_i^T, dP^T = V dO_i^T        (A, B from shared memory, K-major;
 //                                               N = 128: an N = 64 product takes
 //                                               as long as an N = 128 one)
@@ -138,8 +137,7 @@ struct BwdSmem {
   // dS as [key][query]: chunk h holds query columns [64h, 64h+64) of the tile
   alignas(1024) uint8_t ds[kKeys * kRows * 2];
   alignas(16) float stats[2][2][kRows];            // [stage][lse2 | D][row]
-  uint64_t kv_full, q_full[2], q_empty[2], s_full, s_read, pds[2], dq_full, dq_empty, dkv_full,
-      drain;
+  uint64_t kv_full, q_full[2], q_empty[2], s_full, pds[2], dq_full, dq_empty, dkv_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -168,18 +166,19 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
 // WG0 / WG1, each owning 64 of the 128 query columns of every tile.
 //
 // TMEM columns (128 lanes = the CTA's 128 keys):
-//   [0,128)   S^T (query half h in [64h, 64h+64))
-//   [128,256) dP^T; each warpgroup writes its P^T (bf16) over the first 32 columns of
-//             the dP^T half it has read; after the dV products, dQ^T (d = 128: lanes =
-//             head-dim indices, columns = queries) or dQ (d = 64: lanes = queries)
+//   [0,128)   S^T (query half h in [64h, 64h+64)); each warpgroup writes its P^T (bf16)
+//             over the first 32 columns of the S^T half it has read
+//   [128,256) dP^T; once both halves are read, dQ^T (d = 128: lanes = head-dim
+//             indices, columns = queries) or dQ (d = 64: lanes = queries)
 //   [256,256+D) dK accumulator, [256+D,256+2D) dV accumulator
 // Per query tile i the MMA thread issues
-//   (dQ_{i-1} read out) dP^T_i | (S^T_i read out) S^T_{i+1} |
-//   dV += P^T_0 dO_0, dK += dS^T_0 Q_0 | dV += P^T_1 dO_1, dK += dS^T_1 Q_1 | dQ_i = dS K
-// so the next tile's S^T runs while the warpgroups compute P and dS, half 1's P/dS is
-// computed while half 0's products run, and dQ_i's columns are released as soon as
-// the warpgroups have loaded them.  dQ_i overwrites the P^T columns only after the dV
-// products that read them (tcgen05 MMAs of one thread run in issue order).
+//   (dQ_{i-1} read out) dP^T_i | dV += P^T_0 dO_0, dK += dS^T_0 Q_0 | dQ_i |
+//   dV += P^T_1 dO_1, dK += dS^T_1 Q_1 | S^T_{i+1}
+// Writing dQ_i out of the SM is slow and competes with the tensor core for the
+// shared-memory data path; issuing dQ_i as soon as dS is complete lets its read-out
+// and reductions overlap the half-1 products, the next S^T and the next dP^T instead
+// of holding up the next dP^T.  The next S^T overwrites the P^T columns only after the
+// dV products that read them (tcgen05 MMAs of one thread run in issue order).
 //
 // d = 64: dQ leaves through shared memory.  After the dQ product completes, the dS tile
 // has no reader left, so each compute warp stages its 32 query rows x 32 columns of dQ
@@ -218,7 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_init(&sm.pds[s], kKeys);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_read, 2 * kKeys);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_empty, 2 * kKeys);
     mbar_init(&sm.dkv_full, 1);
@@ -295,46 +293,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0);
       }
       mma_commit(&sm.s_full);
-      // the next tile's S^T, as soon as this tile's S^T is in the warpgroups' registers
-      if (it + 1 < nq) {
-        if (!(ok = mbar_wait(&sm.s_read, it & 1, p.status, abort_flag))) break;
-        if (!(ok = mbar_wait(&sm.q_full[s ^ 1], ((it + 1) >> 1) & 1, p.status, abort_flag))) break;
-        tc_fence_after();
-        issue_s(smem_u32(sm.q[s ^ 1]));
-      }
-      // dV += P^T dO and dK += dS^T Q, one query half at a time (K = 64 queries)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        if (!(ok = mbar_wait(&sm.pds[hf], it & 1, p.status, abort_flag))) break;
-        tc_fence_after();
+      // dV += P^T dO and dK += dS^T Q for query half hf (K = 64 queries)
+      auto issue_dkv = [&](int hf) {
 #pragma unroll
         for (int kk = 0; kk < kHalf / 16; ++kk) {
           const uint32_t acc = (it > 0 || hf > 0 || kk > 0) ? 1u : 0u;
           const uint32_t qrow = hf * 8192 + kk * 2048;      // 16 query rows
-          mma_ts(tmem + kColDV, tmem + kColDP + hf * kHalf + kk * 8,
+          mma_ts(tmem + kColDV, tmem + hf * kHalf + kk * 8,
                  sdesc_sw128(do_addr + qrow, 16384, 1024), kIdKV, acc);
           mma_ss(tmem + kColDK, sdesc_sw128(ds_addr + hf * 16384 + kk * 32, 16, 1024),
                  sdesc_sw128(q_addr + qrow, 16384, 1024), kIdKV, acc);
         }
-      }
-      if (!ok) break;
-      // Q_i and dO_i have no reader left: release the stage for tile i + 2's loads
-      mma_commit(&sm.q_empty[s]);
-      // contracting over the 128 keys; K and the dS tile are both read MN-major
+      };
+      if (!(ok = mbar_wait(&sm.pds[0], it & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      issue_dkv(0);
+      if (!(ok = mbar_wait(&sm.pds[1], it & 1, p.status, abort_flag))) break;
+      tc_fence_after();
+      // dQ, contracting over the 128 keys; K and the dS tile are both read MN-major
       if constexpr (D == 128) {
         // dQ^T = K^T dS^T: A = K^T (head-dim contiguous), B = dS^T (queries contiguous)
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           mma_ss(tmem + kColDQ, sdesc_sw128(k_addr + kk * 2048, 16384, 1024),
                  sdesc_sw128(ds_addr + kk * 2048, 16384, 1024), kIdQT, kk > 0);
+        mma_commit(&sm.dq_full);
+        issue_dkv(1);
       } else {
-        // dQ = dS K: A = dS (queries contiguous), B = K (head-dim contiguous)
+        // dQ = dS K: A = dS (queries contiguous), B = K (head-dim contiguous).  The
+        // warpgroups stage dQ in the dS tile, so dq_full waits for dK's last read of it.
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           mma_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
                  sdesc_sw128(k_addr + kk * 2048, 16384, 1024), kIdQ, kk > 0);
+        issue_dkv(1);
+        mma_commit(&sm.dq_full);
       }
-      mma_commit(&sm.dq_full);
+      // Q_i and dO_i have no reader left: release the stage for tile i + 2's loads
+      mma_commit(&sm.q_empty[s]);
+      if (it + 1 < nq) {
+        if (!(ok = mbar_wait(&sm.q_full[s ^ 1], ((it + 1) >> 1) & 1, p.status, abort_flag))) break;
+        tc_fence_after();
+        issue_s(smem_u32(sm.q[s ^ 1]));
+      }
     }
     mma_commit(&sm.dkv_full);
     if (!ok) {
@@ -381,11 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tmem_ld32(lane_base + s_col + c0, sraw);
         tmem_ld32(lane_base + dp_col + c0, draw);
         tmem_ld_wait();
-        if (c0 + 32 == kHalf) {
-          // all of S^T is in registers: the next tile's S^T may overwrite it
-          tc_fence_before();
-          mbar_arrive(&sm.s_read);
-        }
         uint32_t pk[16], dk2[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -401,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           pk[i] = pack_bf16x2(pv[0], pv[1]);
           dk2[i] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        tmem_st16(lane_base + dp_col + c0 / 2, pk);   // over dP^T columns already read
+        tmem_st16(lane_base + s_col + c0 / 2, pk);    // over S^T columns already read
         // dS row into the swizzled [key][query] chunk of this half: 4 x 16-byte units
         const int u0 = c0 / 8;
 #pragma unroll
