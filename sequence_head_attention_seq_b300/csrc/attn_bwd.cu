@@ -7,8 +7,8 @@
 //     dq_i  = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dout_i
 //
 // Three launches:
-//   1. bwd_prep: per query row D_i and lse_i*log2(e) into the workspace (padded
-//      rows get lse = +inf, D = 0 so they contribute nothing), and zero the fp32
+//   1. bwd_prep: per query row D_i and -lse_i*log2(e) into the workspace (padded
+//      and empty rows get -inf, D = 0 so they contribute nothing), and zero the fp32
 //      dQ accumulator.  Bandwidth bound.
 //   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
 //      128-row query tiles that can see it (causal: from the diagonal down).  Two
@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kRows = 128;   // query rows per tile
 constexpr int kKeys = 128;   // keys per CTA
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 two compute warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- 1. row statistics
@@ -84,12 +84,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   float* srow = stats + bh * 2 * rows;
   if (lane == 0) {
-    float l2 = INFINITY;   // padded or empty row: P = exp2(x - inf) = 0
+    float nl2 = -INFINITY;   // padded or empty row: P = exp2(x - inf) = 0
     if (i < sq) {
       const float v = lse[bh * sq + i];
-      if (v != -INFINITY) l2 = v * kLog2e;
+      if (v != -INFINITY) nl2 = -v * kLog2e;
     }
-    srow[i] = l2;
+    srow[i] = nl2;
     srow[rows + i] = (i < sq) ? acc : 0.0f;
   }
   float4* z = reinterpret_cast<float4*>(dq_acc + (bh * rows + i) * D);
@@ -136,7 +136,7 @@ struct BwdSmem {
   alignas(1024) uint8_t dout[2][kTileBytes];
   // dS as [key][query]: chunk h holds query columns [64h, 64h+64) of the tile
   alignas(1024) uint8_t ds[kKeys * kRows * 2];
-  alignas(16) float stats[2][2][kRows];            // [stage][lse2 | D][row]
+  alignas(16) float stats[2][2][kRows];            // [stage][-lse*log2e | D][row]
   uint64_t kv_full, q_full[2], q_empty[2], s_full, pds[2], dq_full, dq_empty, dkv_full, drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -145,7 +145,7 @@ struct BwdSmem {
 struct BwdKernelParams {
   CUtensorMap tq, tk, tv, tdo;
   CUtensorMap tdq;        // fp32 dQ accumulator as [B*H*rows][D], 32 x 32 boxes
-  const float* stats;     // [B][H][2][rows]
+  const float* stats;     // [B][H][2][rows]: -lse*log2(e), D
   float* dq_acc;          // [B][H][rows][D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -162,8 +162,9 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
   return n;
 }
 
-// Threads: warp 0 TMA, warp 1 MMA (+ TMEM), warps 4..7 and 8..11 = compute warpgroups
-// WG0 / WG1, each owning 64 of the 128 query columns of every tile.
+// Threads: warp 0 TMA, warp 1 MMA (+ TMEM), warps 2..5 and 6..9 = compute warpgroups
+// WG0 / WG1, each owning 64 of the 128 query columns of every tile (a warp reaches the
+// TMEM lanes 32 * (warp % 4) .. + 31, so any four consecutive warps cover all 128).
 //
 // TMEM columns (128 lanes = the CTA's 128 keys):
 //   [0,128)   S^T (query half h in [64h, 64h+64)); each warpgroup writes its P^T (bf16)
@@ -343,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       int never = 0;
       mbar_wait(&sm.drain, 0, p.status, &never);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ P / dS, dQ drain, epilogue
-    const int wg = (warp - 4) / 4;                   // query half owned by this warpgroup
+    const int wg = (warp - 2) / 4;                   // query half owned by this warpgroup
     const int quad = warp % 4;
     const int jj = quad * 32 + lane;                 // key row in tile == TMEM lane
     const int key = kv0 + jj;
@@ -369,40 +370,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
       }
-      const float* lse2 = sm.stats[s][0] + wg * kHalf;
+      const float* nlse2 = sm.stats[s][0] + wg * kHalf;   // -lse * log2(e)
       const float* Dv = sm.stats[s][1] + wg * kHalf;
       const int qh0 = q0 + wg * kHalf;               // first query row of this half
       const bool need_mask = (kv0 + kKeys > kvlen) ||
                              (g.causal && kv0 + kKeys - 1 > g.q_offset + qh0);
       // first query column (relative to the half) that sees this key under the causal mask
       const int first_q = g.causal ? key - g.q_offset - qh0 : -(1 << 30);
-#pragma unroll 1
-      for (int c0 = 0; c0 < kHalf; c0 += 32) {
+      const float4* nl4 = reinterpret_cast<const float4*>(nlse2);
+      const float4* D4 = reinterpret_cast<const float4*>(Dv);
+      const uint64_t scale2 = f2_pack(g.scale_log2, g.scale_log2);
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        // 32 columns of S^T and dP^T per round trip to TMEM
         uint32_t sraw[32], draw[32];
-        tmem_ld32(lane_base + s_col + c0, sraw);
-        tmem_ld32(lane_base + dp_col + c0, draw);
+        tmem_ld32(lane_base + s_col + ch * 32, sraw);
+        tmem_ld32(lane_base + dp_col + ch * 32, draw);
         tmem_ld_wait();
         uint32_t pk[16], dk2[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pv[2], dsv[2];
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 l4 = nl4[ch * 8 + i4];
+          const float4 d4 = D4[ch * 8 + i4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = c0 + 2 * i + e;
-            float pr = ex2(fmaf(__uint_as_float(sraw[2 * i + e]), g.scale_log2, -lse2[c]));
-            if (need_mask && (!key_ok || c < first_q)) pr = 0.0f;
-            pv[e] = pr;
-            dsv[e] = pr * (__uint_as_float(draw[2 * i + e]) - Dv[c]);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int cc = i4 * 4 + h2 * 2;            // column pair within the chunk
+            // x = S * scale * log2(e) - lse * log2(e), two columns per instruction
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sraw[cc]),
+                                               __uint_as_float(sraw[cc + 1])),
+                                       scale2, h2 ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y));
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
+            if (need_mask) {
+              const int c = ch * 32 + cc;
+              if (!key_ok || c < first_q) p0 = 0.0f;
+              if (!key_ok || c + 1 < first_q) p1 = 0.0f;
+            }
+            const uint64_t p2 = f2_pack(p0, p1);
+            // dS = P (dP - D)
+            const uint64_t ds2 = f2_mul(
+                p2, f2_sub(f2_pack(__uint_as_float(draw[cc]), __uint_as_float(draw[cc + 1])),
+                           h2 ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y)));
+            float d0, d1;
+            f2_unpack(ds2, d0, d1);
+            pk[i4 * 2 + h2] = pack_bf16x2(p0, p1);
+            dk2[i4 * 2 + h2] = pack_bf16x2(d0, d1);
           }
-          pk[i] = pack_bf16x2(pv[0], pv[1]);
-          dk2[i] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        tmem_st16(lane_base + s_col + c0 / 2, pk);    // over S^T columns already read
+        tmem_st16(lane_base + s_col + ch * 16, pk);    // over S^T columns already read
         // dS row into the swizzled [key][query] chunk of this half: 4 x 16-byte units
-        const int u0 = c0 / 8;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          uint4* dst = reinterpret_cast<uint4*>(ds_row + (((u0 + u) ^ swz) * 16));
+          uint4* dst = reinterpret_cast<uint4*>(ds_row + (((ch * 4 + u) ^ swz) * 16));
           *dst = make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
         }
       }
