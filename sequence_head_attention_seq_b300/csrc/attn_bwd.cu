@@ -26,6 +26,8 @@
 //      contiguous 128-byte piece of a dQ row); for d = 64 staged in the warp's own
 //      slice of the dS tile and added by TMA tensor reduce-adds.
 //   3. bwd_dq_convert: dq = bf16(scale * accumulator).  Bandwidth bound.
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -380,6 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const float4* nl4 = reinterpret_cast<const float4*>(nlse2);
       const float4* D4 = reinterpret_cast<const float4*>(Dv);
       const uint64_t scale2 = f2_pack(g.scale_log2, g.scale_log2);
+      // one copy of the loop per masking case, chosen once per tile (need_mask is uniform
+      // across the warpgroup): no branches inside, so independent column pairs interleave
+      auto p_ds_half = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         // 32 columns of S^T and dP^T per round trip to TMEM
@@ -402,10 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             float x0, x1;
             f2_unpack(x2, x0, x1);
             float p0 = ex2(x0), p1 = ex2(x1);
-            if (need_mask) {
+            if constexpr (kMasked) {
               const int c = ch * 32 + cc;
-              if (!key_ok || c < first_q) p0 = 0.0f;
-              if (!key_ok || c + 1 < first_q) p1 = 0.0f;
+              p0 = (key_ok && c >= first_q) ? p0 : 0.0f;
+              p1 = (key_ok && c + 1 >= first_q) ? p1 : 0.0f;
             }
             const uint64_t p2 = f2_pack(p0, p1);
             // dS = P (dP - D)
@@ -426,6 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           *dst = make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
         }
       }
+      };
+      if (need_mask)
+        p_ds_half(std::true_type{});
+      else
+        p_ds_half(std::false_type{});
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
