@@ -139,7 +139,9 @@ struct BwdSmem {
   // dS as [key][query]: chunk h holds query columns [64h, 64h+64) of the tile
   alignas(1024) uint8_t ds[kKeys * kRows * 2];
   alignas(16) float stats[2][2][kRows];            // [stage][-lse*log2e | D][row]
-  uint64_t kv_full, q_full[2], q_empty[2], s_full, pds[2], dq_full, dq_empty, dkv_full, drain;
+  // q_full: Q tile + row statistics (needed first, by S^T); do_full: dO tile (dP^T, dV)
+  uint64_t kv_full, q_full[2], do_full[2], q_empty[2], s_full, pds[2], dq_full, dq_empty,
+      dkv_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -216,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     mbar_init(&sm.kv_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.do_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
       mbar_init(&sm.pds[s], kKeys);
     }
@@ -253,13 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const int s = it & 1;
       const int q0 = (m_start + it) * kRows;
       if (it >= 2 && !mbar_wait(&sm.q_empty[s], ((it >> 1) - 1) & 1, p.status, abort_flag)) break;
-      mbar_expect_tx(&sm.q_full[s], 2 * kTileBytes + 2 * kRows * 4);
-      for (int c = 0; c < kChunks; ++c) {
+      // Q and the statistics first: the next S^T waits for them, dO is needed later
+      mbar_expect_tx(&sm.q_full[s], kTileBytes + 2 * kRows * 4);
+      for (int c = 0; c < kChunks; ++c)
         tma_load_4d(sm.q[s] + c * 16384, &p.tq, &sm.q_full[s], c * 64, h, q0, b);
-        tma_load_4d(sm.dout[s] + c * 16384, &p.tdo, &sm.q_full[s], c * 64, h, q0, b);
-      }
       bulk_load(sm.stats[s][0], st_base + q0, kRows * 4, &sm.q_full[s]);
       bulk_load(sm.stats[s][1], st_base + p.rows + q0, kRows * 4, &sm.q_full[s]);
+      mbar_expect_tx(&sm.do_full[s], kTileBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_4d(sm.dout[s] + c * 16384, &p.tdo, &sm.do_full[s], c * 64, h, q0, b);
     }
   } else if (warp == 1 && lane == 0 && nq > 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -288,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const uint32_t q_addr = smem_u32(sm.q[s]), do_addr = smem_u32(sm.dout[s]);
       // dP^T overwrites the previous tile's dQ: wait until it has been read out of TMEM
       if (it > 0 && !(ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abort_flag))) break;
+      if (!(ok = mbar_wait(&sm.do_full[s], (it >> 1) & 1, p.status, abort_flag))) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
