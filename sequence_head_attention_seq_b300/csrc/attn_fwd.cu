@@ -228,14 +228,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int j = 0; j < tile.nblocks; ++j) {
       if (!(ok = mbar_wait(&sm.s_full[t], j & 1, p.status, abort_flag))) break;
       tc_fence_after();
+      // the score row in two round trips to TMEM of 64 columns each
       float sv[kKeys];
 #pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) {
-        uint32_t raw[32];
-        tmem_ld32(lane_base + s_col + c * 32, raw);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t raw[2][32];
+        tmem_ld32(lane_base + s_col + h2 * 64, raw[0]);
+        tmem_ld32(lane_base + s_col + h2 * 64 + 32, raw[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(raw[i]);
+        for (int c = 0; c < 64; ++c) sv[h2 * 64 + c] = __uint_as_float(raw[c / 32][c % 32]);
       }
       const int key0 = j * kKeys;
       const bool need_mask = (key0 + kKeys > kvlen) ||
@@ -246,9 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int c = 0; c < kKeys; ++c)
           if (key0 + c >= lim) sv[c] = -INFINITY;
       }
-      float mx = sv[0];
+      // row maximum over eight independent chains (a single chain is 127 dependent steps)
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kKeys; ++c) mx = fmaxf(mx, sv[c]);
+      for (int k = 0; k < 8; ++k) mx8[k] = sv[k];
+#pragma unroll
+      for (int c = 8; c < kKeys; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], sv[c]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx8[k] = fmaxf(mx8[k], mx8[k + 4]);
+      const float mx = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
       const float m_blk = mx * g.scale_log2;
       float m_use = m;
       float alpha = 1.0f;
@@ -275,18 +283,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       l *= alpha;
       m = m_use;
-      const float neg_m = -m;
+      // P = exp2(S * scale * log2(e) - m), two columns per instruction; the row sum
+      // goes into two independent pair accumulators
+      const uint64_t sc2 = f2_pack(g.scale_log2, g.scale_log2);
+      const uint64_t nm2 = f2_pack(-m, -m);
+      uint64_t lsum[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(sv[c * 32 + 2 * i], g.scale_log2, neg_m));
-          const float p1 = ex2(fmaf(sv[c * 32 + 2 * i + 1], g.scale_log2, neg_m));
-          l += p0 + p1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sv[c * 32 + 2 * i], sv[c * 32 + 2 * i + 1]), sc2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          lsum[i & 1] = f2_add(lsum[i & 1], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(lane_base + s_col + c * 16, pk);
+      }
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(lsum[0], a0, a1);
+        f2_unpack(lsum[1], b0, b1);
+        l += (a0 + b0) + (a1 + b1);
       }
       tmem_st_wait();
       tc_fence_before();
