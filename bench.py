@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import contextlib
+import dataclasses
 import hashlib
 import json
 import math
@@ -427,10 +428,17 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="total heads instead of the workload's (same sequence, head dim and "
+                         "shard count; for profiling a smaller case of the same kernels)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     w = workloads.WORKLOADS[args.workload]
+    if args.heads is not None:
+        if args.heads < w.N or args.heads % w.N:
+            ap.error(f"--heads must be a multiple of the shard count {w.N}")
+        w = dataclasses.replace(w, h=args.heads)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
