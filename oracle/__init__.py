@@ -67,9 +67,11 @@ def open_library(path: str):
     lib.oracle_attn_bwd_rows.argtypes = [pp, dp, dp, dp, dp, i, i, i, i, dp, i, i, dp, dp]
     lib.oracle_seq2head.argtypes = [u16, u16, i, i, i, i, i]
     lib.oracle_head2seq.argtypes = [u16, u16, i, i, i, i, i]
+    lib.oracle_attn_merge.argtypes = [i, i, i, i, i, dp, dp, dp, dp]
     lib.oracle_set_threads.argtypes = [i]
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_attn_fwd_rows,
               lib.oracle_attn_bwd_rows, lib.oracle_seq2head, lib.oracle_head2seq,
+              lib.oracle_attn_merge,
               lib.oracle_set_threads, lib.oracle_get_threads):
         f.restype = ctypes.c_int
     return lib
@@ -187,6 +189,19 @@ class Oracle:
             raise ValueError("oracle_attn_bwd_rows rejected the request")
         return dq[: i1 - i0], dk[: j1 - j0], dv[: j1 - j0]
 
+    def attn_merge(self, outs, lses):
+        """Combine per-key-chunk results: outs[k] [B][sq][H][d], lses[k] [B][H][sq] ->
+        (out, lse) of attention over the union of the chunks' keys."""
+        outs = np.ascontiguousarray(np.stack([_f64(o) for o in outs]))
+        lses = np.ascontiguousarray(np.stack([_f64(l) for l in lses]))
+        n, B, sq, H, d = outs.shape
+        out = np.empty((B, sq, H, d), dtype=np.float64)
+        lse = np.empty((B, H, sq), dtype=np.float64)
+        if self.lib.oracle_attn_merge(B, H, sq, d, n, _ptr(outs), _ptr(lses), _ptr(out),
+                                      _ptr(lse)):
+            raise ValueError("oracle_attn_merge rejected the request")
+        return out, lse
+
     def seq2head(self, x, N, b, s, h, d) -> np.ndarray:
         """[N][b][s/N][h][d] -> [N][b][s][h/N][d], as opaque 16-bit words."""
         x = _u16(x)
@@ -216,6 +231,6 @@ def default() -> Oracle:
 def __getattr__(name):
     # module-level shortcuts: oracle.attn_fwd(...), oracle.seq2head(...), ...
     if name in ("set_threads", "threads", "attn_fwd", "attn_bwd", "attn_fwd_rows",
-                "attn_bwd_rows", "seq2head", "head2seq"):
+                "attn_bwd_rows", "attn_merge", "seq2head", "head2seq"):
         return getattr(default(), name)
     raise AttributeError(name)

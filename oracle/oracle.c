@@ -465,3 +465,47 @@ int oracle_head2seq(const uint16_t* in, uint16_t* out, int N, int b, int s, int 
                     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Ring / blockwise attention: combine per-key-chunk results.          */
+/* "adv07: Sequence Parallel", sections 5 and 7: K/V blocks travel a   */
+/* ring and each device attends to one block at a time.  The pages     */
+/* give no combination formula; the softmax over a union of disjoint   */
+/* key sets is, row by row, with m = max_k lse_k:                      */
+/*     lse = m + log(sum_k exp(lse_k - m))                             */
+/*     out = sum_k exp(lse_k - lse) * out_k                            */
+/* A chunk with lse_k = -inf contributes nothing; all -inf gives       */
+/* out = 0, lse = -inf.                                                */
+/* outs: [nparts][B][sq][H][d], lses: [nparts][B][H][sq]; results in   */
+/* out [B][sq][H][d] and lse [B][H][sq].                               */
+/* ------------------------------------------------------------------ */
+
+int oracle_attn_merge(int B, int H, int sq, int d, int nparts, const double* outs,
+                      const double* lses, double* out, double* lse)
+{
+    if (B < 0 || H < 0 || sq < 0 || d <= 0 || nparts < 1) return 1;
+    const size_t out_part = (size_t)B * sq * H * d, lse_part = (size_t)B * H * sq;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int i = 0; i < sq; ++i) {
+                const size_t li = ((size_t)b * H + h) * sq + i;
+                const size_t oi = (((size_t)b * sq + i) * H + h) * d;
+                double m = -INFINITY;
+                for (int k = 0; k < nparts; ++k)
+                    if (lses[k * lse_part + li] > m) m = lses[k * lse_part + li];
+                for (int c = 0; c < d; ++c) out[oi + c] = 0.0;
+                if (m == -INFINITY) {
+                    lse[li] = -INFINITY;
+                    continue;
+                }
+                double s = 0.0;
+                for (int k = 0; k < nparts; ++k) s += exp(lses[k * lse_part + li] - m);
+                const double total = m + log(s);
+                lse[li] = total;
+                for (int k = 0; k < nparts; ++k) {
+                    const double w = exp(lses[k * lse_part + li] - total);
+                    for (int c = 0; c < d; ++c) out[oi + c] += w * outs[k * out_part + oi + c];
+                }
+            }
+    return 0;
+}

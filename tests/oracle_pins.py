@@ -382,10 +382,60 @@ def pin_relayout_torch(orc):
         assert np.array_equal(back, x.numpy().view(np.uint16))
 
 
+def _chunk_key_len(key_len, lo, hi):
+    """Valid keys of chunk [lo, hi) given the full key_len per batch entry."""
+    if key_len is None:
+        return None
+    return [min(max(n - lo, 0), hi - lo) for n in key_len]
+
+
+def pin_merge_split_kv(orc):
+    """adv07 tutorial sections 5 and 7 (ring / blockwise attention): attention against
+    each key chunk, the query position taken relative to the chunk's first key, merged by
+    the log-sum-exp rule equals attention against all keys.  Chunks are ragged; some
+    rows see no key of a chunk, and one batch entry has no visible key at all."""
+    B, H, sq, sk, d = 2, 2, 23, 41, 8
+    q, k, v = _rand((B, sq, H, d), 170), _rand((B, sk, H, d), 171), _rand((B, sk, H, d), 172)
+    bounds = [(0, 7), (7, 20), (20, 33), (33, 41)]
+    for causal, q_offset, key_len in ((True, 18, None), (True, 0, [41, 0]),
+                                      (False, 0, [41, 12]), (False, 0, None)):
+        full, full_lse = orc.attn_fwd(q, k, v, causal, q_offset, key_len)
+        outs, lses = [], []
+        for lo, hi in bounds:
+            o, l = orc.attn_fwd(q, k[:, lo:hi], v[:, lo:hi], causal, q_offset - lo,
+                                _chunk_key_len(key_len, lo, hi))
+            outs.append(o)
+            lses.append(l)
+        out, lse = orc.attn_merge(outs, lses)
+        _close(out, full, 1e-12, f"merged out causal={causal}")
+        fin = np.isfinite(full_lse)
+        assert np.array_equal(np.isfinite(lse), fin)
+        _close(lse[fin], full_lse[fin], 1e-12, f"merged lse causal={causal}")
+        # merging is order-free
+        rev, rev_lse = orc.attn_merge(outs[::-1], lses[::-1])
+        _close(rev, out, 1e-13, "merge order")
+
+
+def pin_merge_closed_forms(orc):
+    """Two copies of one result: same out, lse + ln 2.  An empty partial (lse = -inf)
+    changes nothing.  All partials empty: out 0, lse -inf."""
+    B, H, sq, d = 1, 2, 5, 4
+    o = _rand((B, sq, H, d), 180)
+    lse = _rand((B, H, sq), 181)
+    out, l2 = orc.attn_merge([o, o], [lse, lse])
+    _close(out, o, 1e-14, "duplicate out")
+    _close(l2, lse + math.log(2.0), 1e-14, "duplicate lse")
+    empty_lse = np.full_like(lse, -np.inf)
+    out, l1 = orc.attn_merge([o, np.zeros_like(o)], [lse, empty_lse])
+    assert np.array_equal(out, o) and np.array_equal(l1, lse)
+    out, l0 = orc.attn_merge([np.zeros_like(o)] * 2, [empty_lse, empty_lse])
+    assert not out.any() and np.all(l0 == -np.inf)
+
+
 ALL_PINS = [
     pin_sdpa_causal_square, pin_sdpa_masks, pin_finite_differences, pin_zero_q_uniform,
     pin_causal_row0, pin_constant_v, pin_one_and_two_keys, pin_softmax_rows,
     pin_key_padding_is_truncation, pin_gradient_sums, pin_empty_rows, pin_rows_api,
     pin_golden_causal_example, pin_golden_split_q, pin_negative_control,
-    pin_relayout_golden, pin_relayout_torch,
+    pin_relayout_golden, pin_relayout_torch, pin_merge_split_kv, pin_merge_closed_forms,
 ]

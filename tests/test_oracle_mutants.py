@@ -39,6 +39,9 @@ MUTANTS = {
                             "const int r = t / sl, u = t % sl, head = j * N + g;"),
     "shards_interleaved": ("const int r = t / sl, u = t % sl, head = g * hl + j;",
                            "const int r = t % N, u = t / N, head = g * hl + j;"),
+    "merge_weight_unnormalised": ("const double w = exp(lses[k * lse_part + li] - total);",
+                                  "const double w = exp(lses[k * lse_part + li] - m);"),
+    "merge_lse_drops_max": ("const double total = m + log(s);", "const double total = log(s);"),
     "head2seq_groups_strided": ("const int g = head / hl, j = head % hl, t = r * sl + u;",
                                 "const int g = head % N, j = head / N, t = r * sl + u;"),
 }
