@@ -81,7 +81,11 @@ sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int nten
  * from (input_ids != pad).
  *
  * Key j is visible from query row i of batch entry bb iff
- *     (!causal || j <= q_offset + i)  &&  (key_len == NULL || j < key_len[bb]).
+ *     (!causal || kv_offset + j <= q_offset + i)  &&  (key_len == NULL || j < key_len[bb]).
+ * q_offset and kv_offset are the global sequence positions of query row 0 and key
+ * row 0: a query shard (split-Q) sets q_offset, a key chunk of ring / blockwise
+ * attention sets kv_offset ("adv07: Sequence Parallel", sections 5 and 7: K/V blocks
+ * passed around a ring, each device attending to one block at a time).
  * A row with no visible key returns out = 0, lse = -inf and no gradient.
  *
  * Layout: q, o, dout, dq are [B][sq][H][d]; k, v, dk, dv are [B][sk][H][d];
@@ -101,8 +105,10 @@ typedef struct sp_attn_params {
     int d;                    /* head_dim: 64 or 128 */
     int causal;               /* 0 or 1 */
     int q_offset;             /* global sequence position of query row 0 (>= 0) */
+    int kv_offset;            /* global sequence position of key row 0 (>= 0) */
     const int32_t* key_len;   /* NULL, or DEVICE [B] valid-key counts in [0, sk] */
     float softmax_scale;      /* <= 0 selects 1/sqrt(d) */
+    int dq_accumulate;        /* sp_attn_bwd only, 0 or 1: see sp_attn_bwd */
 } sp_attn_params;
 
 /*
@@ -112,10 +118,11 @@ typedef struct sp_attn_params {
  *
  * o   : DEVICE bf16, layout of q with o_stride.
  * lse : DEVICE fp32 [B][H][sq], contiguous.  Needed by sp_attn_bwd.
- * Errors: B, H, sq, sk < 0 or any of them 0 with others nonzero is allowed
- *         (nothing to do -> SP_OK); causal with q_offset + sq > sk, q_offset < 0,
- *         NULL pointers -> SP_ERR_INVALID_ARG; d not 64/128 -> SP_ERR_UNSUPPORTED;
- *         pointer/stride alignment -> SP_ERR_MISALIGNED.
+ * Errors: B, H, sq, sk < 0, q_offset < 0, kv_offset < 0, causal not 0/1, NULL
+ *         pointers -> SP_ERR_INVALID_ARG (B, H, sq or sk equal to 0 is allowed:
+ *         nothing to do, SP_OK); d not 64/128, q_offset + sq or kv_offset + sk
+ *         above 2^30 -> SP_ERR_UNSUPPORTED; pointer/stride alignment ->
+ *         SP_ERR_MISALIGNED.
  */
 sp_status sp_attn_fwd(const sp_attn_params* p, void* o, float* lse, void* stream);
 
@@ -135,12 +142,61 @@ size_t sp_attn_bwd_workspace_size(const sp_attn_params* p);
  *
  * o, lse     : the forward's outputs for the same p.
  * workspace  : DEVICE, >= sp_attn_bwd_workspace_size(p) bytes, 256-byte aligned,
- *              owned by the caller; its contents on entry do not matter.
+ *              owned by the caller; its contents on entry do not matter unless
+ *              p->dq_accumulate is set.
+ * dq_accumulate = 1 (ring / blockwise attention, one call per key chunk with that
+ *              chunk's k, v and kv_offset, and the merged o and lse): this call's dq
+ *              contribution is added to the fp32 accumulator the previous call left in
+ *              the same workspace (same B, H, sq, d), and dq receives the running sum.
+ *              The first chunk's call uses dq_accumulate = 0.  dk and dv are always
+ *              this call's (this chunk's) gradients.
  * Errors as sp_attn_fwd, plus SP_ERR_WORKSPACE when workspace_bytes is too small.
  */
 sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse,
                       const void* dout, void* dq, void* dk, void* dv, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/*
+ * Ring / blockwise attention: merge the result of one key chunk into a running
+ * accumulator.  "adv07: Sequence Parallel", section 5 (Ring Attention passes K/V
+ * blocks around a ring, each device computing attention against one block at a time,
+ * "like a distributed chunked prefill") and section 7.  The pages give no formula for
+ * combining the blocks; this is the plain identity for a softmax split over disjoint
+ * key sets, with per-chunk results (o_c, lse_c) from sp_attn_fwd (kv_offset = chunk
+ * start):
+ *     lse = log(exp(lse_acc) + exp(lse_part))
+ *     o   = exp(lse_acc - lse) * o_acc + exp(lse_part - lse) * o_part
+ * (a side with lse = -inf, no visible key, has weight 0; both -inf gives o = 0,
+ * lse = -inf).  fp32 arithmetic.
+ *
+ * All pointers are DEVICE memory owned by the caller; rows are (bb, i, h) for
+ * bb < B, i < sq, h < H, with head_dim d in {64, 128} contiguous:
+ *   o_part   : bf16, element (bb, i, h, c) at bb*part_stride[0] + i*part_stride[1]
+ *              + h*part_stride[2] + c (strides in elements, multiples of 8)
+ *   lse_part : fp32 [B][H][sq] contiguous
+ *   o_acc    : fp32 [B][sq][H][d] contiguous, updated in place
+ *   lse_acc  : fp32 [B][H][sq] contiguous, updated in place
+ *   o_out    : NULL, or bf16 with out_stride: also receives the merged output
+ *              rounded to bf16 (nearest even), for the last chunk
+ * init != 0 starts a new accumulation: o_acc and lse_acc are overwritten with the
+ * partial (their contents on entry are not read).
+ * Errors: sizes < 0, d not 64/128 -> SP_ERR_INVALID_ARG / SP_ERR_UNSUPPORTED; NULL
+ * required pointers -> SP_ERR_INVALID_ARG; pointers not 16-byte aligned or strides
+ * not multiples of 8 -> SP_ERR_MISALIGNED.
+ */
+typedef struct sp_merge_params {
+    int B, H, sq, d;
+    int init;
+    const void* o_part;
+    int64_t part_stride[3];
+    const float* lse_part;
+    float* o_acc;
+    float* lse_acc;
+    void* o_out;
+    int64_t out_stride[3];
+} sp_merge_params;
+
+sp_status sp_attn_merge(const sp_merge_params* p, void* stream);
 
 /* Size of the device scratch array that sp_attn_bwd_noalloc uses (32 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -157,6 +213,8 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse,
  *
  *  - Problems whose workspace (sp_attn_bwd_workspace_size) exceeds
  *    SP_NOALLOC_SCRATCH_BYTES are rejected with SP_ERR_WORKSPACE before any launch.
+ *  - dq_accumulate must be 0 (SP_ERR_INVALID_ARG otherwise): the shared scratch does
+ *    not carry an accumulation from one call to the next.
  *  - The first call on each device looks up the array's device address (with that
  *    device current); make that first call before capturing any stream.
  *  - All calls share the one array per device and it keeps whatever the last call

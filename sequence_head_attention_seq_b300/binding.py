@@ -28,7 +28,7 @@ MAX_RELAYOUT_TENSORS = 8
 
 # Every symbol include/sp.h declares.
 EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_attn_fwd",
-           "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_bwd_noalloc",
+           "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_merge", "sp_attn_bwd_noalloc",
            "sp_get_device_status", "sp_status_string"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # SP_NOALLOC_SCRATCH_BYTES
 
@@ -47,7 +47,20 @@ class SpAttnParams(ctypes.Structure):
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
         ("B", ctypes.c_int), ("H", ctypes.c_int), ("sq", ctypes.c_int), ("sk", ctypes.c_int),
         ("d", ctypes.c_int), ("causal", ctypes.c_int), ("q_offset", ctypes.c_int),
+        ("kv_offset", ctypes.c_int),
         ("key_len", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
+        ("dq_accumulate", ctypes.c_int),
+    ]
+
+
+class SpMergeParams(ctypes.Structure):
+    """Mirror of sp_merge_params."""
+    _fields_ = [
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("sq", ctypes.c_int), ("d", ctypes.c_int),
+        ("init", ctypes.c_int),
+        ("o_part", ctypes.c_void_p), ("part_stride", ctypes.c_int64 * 3),
+        ("lse_part", ctypes.c_void_p), ("o_acc", ctypes.c_void_p), ("lse_acc", ctypes.c_void_p),
+        ("o_out", ctypes.c_void_p), ("out_stride", ctypes.c_int64 * 3),
     ]
 
 
@@ -86,6 +99,8 @@ def load(build_if_missing: bool = True):
         lib.sp_attn_bwd.restype = i
         lib.sp_attn_bwd_noalloc.argtypes = [pp] + [ctypes.c_void_p] * 7
         lib.sp_attn_bwd_noalloc.restype = i
+        lib.sp_attn_merge.argtypes = [ctypes.POINTER(SpMergeParams), ctypes.c_void_p]
+        lib.sp_attn_merge.restype = i
         lib.sp_get_device_status.argtypes = [ctypes.c_void_p]
         lib.sp_get_device_status.restype = i
         lib.sp_status_string.argtypes = [i]
@@ -177,7 +192,7 @@ def _strides(t: torch.Tensor, name: str):
 
 
 def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
-                softmax_scale=None) -> SpAttnParams:
+                softmax_scale=None, kv_offset: int = 0) -> SpAttnParams:
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need_bf16_cuda(name, t)
     B, sq, H, d = q.shape
@@ -192,6 +207,7 @@ def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
     p.B, p.H, p.sq, p.sk, p.d = B, H, sq, k.shape[1], d
     p.causal = 1 if causal else 0
     p.q_offset = int(q_offset)
+    p.kv_offset = int(kv_offset)
     if key_len is not None:
         if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != B:
             raise ValueError("key_len must be a CUDA int32 tensor of B entries")
@@ -203,7 +219,7 @@ def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
 
 
 def sp_attn_fwd(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
-                softmax_scale=None, out=None, lse=None):
+                softmax_scale=None, out=None, lse=None, kv_offset: int = 0):
     """out [B][sq][H][d] bf16 and lse [B][H][sq] fp32 (natural log)."""
     lib = load()
     B, sq, H, d = q.shape
@@ -214,28 +230,35 @@ def sp_attn_fwd(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
     _need_bf16_cuda("out", out)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, sq):
         raise ValueError("lse must be contiguous fp32 [B][H][sq]")
-    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale)
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset)
     rc = lib.sp_attn_fwd(ctypes.byref(p), out.data_ptr(), lse.data_ptr(), _stream(q.device))
     _check("sp_attn_fwd", rc)
     return out, lse
 
 
 def sp_attn_bwd_workspace_size(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
-                               softmax_scale=None) -> int:
+                               softmax_scale=None, kv_offset: int = 0) -> int:
     lib = load()
-    p = make_params(q, k, v, q, causal, q_offset, key_len, softmax_scale)
+    p = make_params(q, k, v, q, causal, q_offset, key_len, softmax_scale, kv_offset)
     return int(lib.sp_attn_bwd_workspace_size(ctypes.byref(p)))
 
 
 def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0, key_len=None,
-                softmax_scale=None, dq=None, dk=None, dv=None, workspace=None):
-    """dq, dk, dv (bf16, layouts of q, k, v) from the forward's out/lse and dout."""
+                softmax_scale=None, dq=None, dk=None, dv=None, workspace=None,
+                kv_offset: int = 0, dq_accumulate: bool = False):
+    """dq, dk, dv (bf16, layouts of q, k, v) from the forward's out/lse and dout.
+
+    Ring / blockwise attention: call once per key chunk (k, v of the chunk, its
+    kv_offset, the merged out/lse), with dq_accumulate=True after the first chunk and
+    the same workspace each time; dq then holds the sum over the chunks so far."""
     lib = load()
     _need_bf16_cuda("out", out)
     _need_bf16_cuda("dout", dout)
     if out.shape != dout.shape or not _same_layout(out, dout):
         raise ValueError("out and dout must share shape and strides")
-    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale)
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset)
+    p.dq_accumulate = 1 if dq_accumulate else 0
+
     def like(t):
         return torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=t.device)
 
@@ -248,6 +271,8 @@ def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
             raise ValueError(f"{name} must have the shape and strides of its input")
     need = int(lib.sp_attn_bwd_workspace_size(ctypes.byref(p)))
     if workspace is None:
+        if dq_accumulate:
+            raise ValueError("dq_accumulate needs the workspace of the previous call")
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = lib.sp_attn_bwd(ctypes.byref(p), out.data_ptr(), lse.data_ptr(), dout.data_ptr(),
                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
@@ -257,7 +282,8 @@ def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
 
 
 def sp_attn_bwd_noalloc(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
-                        key_len=None, softmax_scale=None, dq=None, dk=None, dv=None):
+                        key_len=None, softmax_scale=None, dq=None, dk=None, dv=None,
+                        kv_offset: int = 0):
     """sp_attn_bwd with the library's own fixed device scratch instead of a workspace.
 
     For callers that must not allocate device memory during the call: the C entry
@@ -271,7 +297,7 @@ def sp_attn_bwd_noalloc(q, k, v, out, lse, dout, causal: bool = True, q_offset: 
     _need_bf16_cuda("dout", dout)
     if out.shape != dout.shape or not _same_layout(out, dout):
         raise ValueError("out and dout must share shape and strides")
-    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale)
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset)
 
     def like(t):
         return torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=t.device)
@@ -288,6 +314,39 @@ def sp_attn_bwd_noalloc(q, k, v, out, lse, dout, causal: bool = True, q_offset: 
                                  _stream(q.device))
     _check("sp_attn_bwd_noalloc", rc)
     return dq, dk, dv
+
+
+def sp_attn_merge(o_part, lse_part, o_acc, lse_acc, init: bool, o_out=None):
+    """Merge one key chunk's (o_part bf16 [B][sq][H][d], lse_part fp32 [B][H][sq]) into
+    the running (o_acc fp32 [B][sq][H][d], lse_acc fp32 [B][H][sq]) in place; init starts a
+    new accumulation; o_out (bf16, layout of o_part) also receives the merged output."""
+    lib = load()
+    _need_bf16_cuda("o_part", o_part)
+    B, sq, H, d = o_part.shape
+    for name, t, shape in (("lse_part", lse_part, (B, H, sq)), ("o_acc", o_acc, (B, sq, H, d)),
+                           ("lse_acc", lse_acc, (B, H, sq))):
+        if (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()
+                or tuple(t.shape) != shape):
+            raise ValueError(f"{name} must be contiguous CUDA fp32 of shape {shape}")
+    p = SpMergeParams()
+    p.B, p.H, p.sq, p.d = B, H, sq, d
+    p.init = 1 if init else 0
+    p.o_part = o_part.data_ptr()
+    p.part_stride = _strides(o_part, "o_part")
+    p.lse_part = lse_part.data_ptr()
+    p.o_acc = o_acc.data_ptr()
+    p.lse_acc = lse_acc.data_ptr()
+    if o_out is not None:
+        _need_bf16_cuda("o_out", o_out)
+        if o_out.shape != o_part.shape:
+            raise ValueError("o_out must have the shape of o_part")
+        p.o_out = o_out.data_ptr()
+        p.out_stride = _strides(o_out, "o_out")
+    else:
+        p.o_out = None
+    rc = lib.sp_attn_merge(ctypes.byref(p), _stream(o_part.device))
+    _check("sp_attn_merge", rc)
+    return o_acc, lse_acc
 
 
 def sp_get_device_status(device=None) -> int:

@@ -24,7 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsp.so")
 
-SOURCES = ["sp_abi.cu", "relayout.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_noalloc.cu"]
+SOURCES = ["sp_abi.cu", "relayout.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_merge.cu",
+           "attn_bwd_noalloc.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

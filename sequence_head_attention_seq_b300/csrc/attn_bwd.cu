@@ -9,7 +9,8 @@
 // Three launches:
 //   1. bwd_prep: per query row D_i and -lse_i*log2(e) into the workspace (padded
 //      and empty rows get -inf, D = 0 so they contribute nothing), and zero the fp32
-//      dQ accumulator.  Bandwidth bound.
+//      dQ accumulator unless the call continues an accumulation over key chunks.
+//      Bandwidth bound.
 //   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
 //      128-row query tiles that can see it (causal: from the diagonal down).  Two
 //      compute warpgroups each own 64 of a tile's query columns.
@@ -94,9 +95,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     srow[i] = nl2;
     srow[rows + i] = (i < sq) ? acc : 0.0f;
   }
-  float4* z = reinterpret_cast<float4*>(dq_acc + (bh * rows + i) * D);
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = lane; c < D / 4; c += 32) z[c] = zero;
+  if (dq_acc != nullptr) {   // null: keep the previous call's accumulator
+    float4* z = reinterpret_cast<float4*>(dq_acc + (bh * rows + i) * D);
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = lane; c < D / 4; c += 32) z[c] = zero;
+  }
 }
 
 // ---------------------------------------------------------------- 3. dQ convert
@@ -560,12 +563,14 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
       if (g.d == 128)
         bwd_prep_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout),
-            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats, a.dq_acc, g.B, g.H,
+            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats,
+            a.dq_accumulate ? nullptr : a.dq_acc, g.B, g.H,
             g.sq, rows);
       else
         bwd_prep_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout),
-            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats, a.dq_acc, g.B, g.H,
+            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats,
+            a.dq_accumulate ? nullptr : a.dq_acc, g.B, g.H,
             g.sq, rows);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

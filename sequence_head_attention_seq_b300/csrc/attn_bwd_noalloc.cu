@@ -45,6 +45,8 @@ void* scratch_address() {
 extern "C" sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o,
                                          const float* lse, const void* dout, void* dq, void* dk,
                                          void* dv, void* stream) {
+  // the shared scratch carries no accumulation from one call to the next
+  if (p != nullptr && p->dq_accumulate != 0) return SP_ERR_INVALID_ARG;
   const size_t need = sp_attn_bwd_workspace_size(p);
   if (need == 0) {
     // invalid parameters, or a problem that needs no workspace: the regular entry

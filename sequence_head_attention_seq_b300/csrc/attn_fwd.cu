@@ -3,7 +3,8 @@
 // What it computes ("adv07: Sequence Parallel" tutorial, section 3 Q4 and
 // section 4; "Parallel multi-head attention", section 3.2):
 //     out[i] = softmax(scale * q[i] K^T + mask) V,   lse[i] = log sum_j exp(scale q[i].k_j)
-// over the visible keys j (j <= q_offset + i when causal, j < key_len[b]).
+// over the visible keys j (j <= q_offset + i when causal, q_offset being query row
+// 0's position relative to key row 0; j < key_len[b]).
 //
 // Design (one CTA = two 128-row query tiles of one (batch entry, head)):
 //   warp 0        TMA producer: Q tiles once, then K/V blocks through a 2-stage ring
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t o_col = kOCol0 + t * D;
     const TileInfo tile = ti[t];
     const int qrow = tile.q0 + r;                    // local query row
-    const int gq = g.q_offset + qrow;                // global position (causal mask)
+    const int gq = g.q_offset + qrow;                // position relative to key row 0
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < tile.nblocks; ++j) {
@@ -286,7 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // P = exp2(S * scale * log2(e) - m), two columns per instruction; the row sum
       // goes into two independent pair accumulators
       const uint64_t sc2 = f2_pack(g.scale_log2, g.scale_log2);
-      const uint64_t nm2 = f2_pack(-m, -m);
+      // a row that sees no key of this tile so far keeps m = -inf; its P must be 0
+      const float nm = (m == -INFINITY) ? 0.0f : -m;
+      const uint64_t nm2 = f2_pack(nm, nm);
       uint64_t lsum[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {

@@ -17,7 +17,8 @@ cudaError_t launch_relayout(const void* const* in, void* const* out, int ntensor
 // Problem geometry after validation (see sp_attn_params).
 struct AttnGeom {
   int B, H, sq, sk, d;
-  int causal, q_offset;
+  int causal;
+  int q_offset;               // query row 0's position relative to key row 0 (may be < 0)
   const int32_t* key_len;     // device, may be null
   float scale;                // softmax scale
   float scale_log2;           // scale * log2(e)
@@ -57,10 +58,25 @@ struct BwdArgs {
   void* dv;
   int64_t q_stride[3], k_stride[3], v_stride[3];
   float* dq_acc;      // workspace: [B][H][rows][d] fp32
-  float* row_stats;   // workspace: [B][H][2][rows] fp32 (lse*log2e, D)
+  float* row_stats;   // workspace: [B][H][2][rows] fp32 (-lse*log2e, D)
+  bool dq_accumulate; // keep dq_acc from the previous call instead of zeroing it
   AttnGeom g;
   uint32_t* status;
 };
 cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
+
+// Merge of one key chunk's attention result into a running accumulator (sp_attn_merge).
+struct MergeArgs {
+  int B, H, sq, d;
+  int init;
+  const void* o_part;
+  int64_t part_stride[3];
+  const float* lse_part;
+  float* o_acc;
+  float* lse_acc;
+  void* o_out;            // may be null
+  int64_t out_stride[3];
+};
+cudaError_t launch_attn_merge(const MergeArgs& a, cudaStream_t stream);
 
 }  // namespace sp

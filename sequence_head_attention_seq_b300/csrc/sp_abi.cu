@@ -87,9 +87,12 @@ sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
   if (p == nullptr) return SP_ERR_INVALID_ARG;
   if (p->B < 0 || p->H < 0 || p->sq < 0 || p->sk < 0) return SP_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return SP_ERR_INVALID_ARG;
-  if (p->q_offset < 0) return SP_ERR_INVALID_ARG;
+  if (p->dq_accumulate != 0 && p->dq_accumulate != 1) return SP_ERR_INVALID_ARG;
+  if (p->q_offset < 0 || p->kv_offset < 0) return SP_ERR_INVALID_ARG;
   if (p->d != 64 && p->d != 128) return SP_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(p->q_offset) + p->sq > (int64_t(1) << 30)) return SP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->q_offset) + p->sq > (int64_t(1) << 30) ||
+      static_cast<int64_t>(p->kv_offset) + p->sk > (int64_t(1) << 30))
+    return SP_ERR_UNSUPPORTED;
   if (p->q == nullptr || p->k == nullptr || p->v == nullptr) return SP_ERR_INVALID_ARG;
   if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v)) return SP_ERR_MISALIGNED;
   if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride) || !strides_ok(p->v_stride) ||
@@ -102,7 +105,9 @@ sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
   g->sk = p->sk;
   g->d = p->d;
   g->causal = p->causal;
-  g->q_offset = p->q_offset;
+  // the kernels mask by the query position relative to key row 0 (may be negative:
+  // query rows before a key chunk's start see none of its keys)
+  g->q_offset = p->q_offset - p->kv_offset;
   g->key_len = p->key_len;
   float scale = p->softmax_scale;
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(p->d));
@@ -246,6 +251,7 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
   a.dv = dv;
   a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.dq_off);
   a.row_stats = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.stats_off);
+  a.dq_accumulate = p->dq_accumulate != 0;
   if (g.sq > 0 && g.sk > 0 &&
       !encode_acc_map(&a.tdq, a.dq_acc, g.d,
                       static_cast<int64_t>(g.B) * g.H * padded_rows(g.sq)))
@@ -254,6 +260,39 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
   a.status = status_word();
   if (a.status == nullptr) return SP_ERR_CUDA;
   return launch_attn_bwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+sp_status sp_attn_merge(const sp_merge_params* p, void* stream) {
+  if (p == nullptr) return SP_ERR_INVALID_ARG;
+  if (p->B < 0 || p->H < 0 || p->sq < 0) return SP_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return SP_ERR_UNSUPPORTED;
+  if (p->o_part == nullptr || p->lse_part == nullptr || p->o_acc == nullptr ||
+      p->lse_acc == nullptr)
+    return SP_ERR_INVALID_ARG;
+  if (!aligned16(p->o_part) || !aligned16(p->o_acc) || !strides_ok(p->part_stride) ||
+      (reinterpret_cast<uintptr_t>(p->lse_part) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(p->lse_acc) & 3u) != 0)
+    return SP_ERR_MISALIGNED;
+  if (p->o_out != nullptr && (!aligned16(p->o_out) || !strides_ok(p->out_stride)))
+    return SP_ERR_MISALIGNED;
+  if (p->B == 0 || p->H == 0 || p->sq == 0) return SP_OK;
+  MergeArgs a;
+  a.B = p->B;
+  a.H = p->H;
+  a.sq = p->sq;
+  a.d = p->d;
+  a.init = p->init != 0;
+  a.o_part = p->o_part;
+  a.lse_part = p->lse_part;
+  a.o_acc = p->o_acc;
+  a.lse_acc = p->lse_acc;
+  a.o_out = p->o_out;
+  for (int i = 0; i < 3; ++i) {
+    a.part_stride[i] = p->part_stride[i];
+    a.out_stride[i] = p->out_stride[i];
+  }
+  return launch_attn_merge(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SP_OK
+                                                                                 : SP_ERR_CUDA;
 }
 
 sp_status sp_get_device_status(void* stream) {

@@ -14,7 +14,7 @@ import contextlib
 
 import torch
 
-from .binding import (sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd,
+from .binding import (sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd, sp_attn_merge,
                       sp_relayout_head2seq, sp_relayout_seq2head)
 
 
@@ -88,3 +88,54 @@ class UlyssesAttention:
         self._to_shards((self.dqg, self.dkg, self.dvg), (self.dq, self.dk, self.dv),
                         "head2seq_grads")
         return self.dq, self.dk, self.dv
+
+
+def _chunk_key_len(key_len, lo, hi):
+    """Valid keys of the key chunk [lo, hi) for each batch entry (device int32)."""
+    if key_len is None:
+        return None
+    return (key_len.to(torch.int32) - lo).clamp_(0, hi - lo).contiguous()
+
+
+def ring_attention_fwd(q, k, v, chunks, causal=True, q_offset=0, key_len=None,
+                       softmax_scale=None):
+    """Blockwise (ring) attention on one GPU: the keys are visited chunk by chunk, as the
+    K/V blocks of a ring arrive at one device ("adv07: Sequence Parallel", sections 5
+    and 7), and each chunk's (o, lse) is merged into an fp32 accumulator.
+
+    q [B][sq][H][d], k/v [B][sk][H][d]; chunks = [(lo, hi), ...] partitioning [0, sk)
+    in visiting order.  Returns (out bf16, lse fp32, o_acc fp32)."""
+    B, sq, H, d = q.shape
+    part = torch.empty_like(q, memory_format=torch.contiguous_format)
+    part_lse = torch.empty((B, H, sq), dtype=torch.float32, device=q.device)
+    o_acc = torch.empty((B, sq, H, d), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B, H, sq), dtype=torch.float32, device=q.device)
+    out = torch.empty_like(part)
+    for n, (lo, hi) in enumerate(chunks):
+        sp_attn_fwd(q, k[:, lo:hi], v[:, lo:hi], causal, q_offset,
+                    _chunk_key_len(key_len, lo, hi), softmax_scale, out=part, lse=part_lse,
+                    kv_offset=lo)
+        sp_attn_merge(part, part_lse, o_acc, lse, init=(n == 0),
+                      o_out=out if n == len(chunks) - 1 else None)
+    return out, lse, o_acc
+
+
+def ring_attention_bwd(q, k, v, out, lse, dout, chunks, causal=True, q_offset=0, key_len=None,
+                       softmax_scale=None):
+    """Backward of ring_attention_fwd, chunk by chunk with the merged out and lse: each
+    chunk's call yields that chunk's dk, dv and adds its dq contribution to an fp32
+    accumulator kept in the shared workspace."""
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = None
+    for n, (lo, hi) in enumerate(chunks):
+        kl = _chunk_key_len(key_len, lo, hi)
+        if ws is None:
+            size = sp_attn_bwd_workspace_size(q, k[:, lo:hi], v[:, lo:hi], causal, q_offset, kl,
+                                              softmax_scale, kv_offset=lo)
+            ws = torch.empty(max(size, 1), dtype=torch.uint8, device=q.device)
+        sp_attn_bwd(q, k[:, lo:hi], v[:, lo:hi], out, lse, dout, causal, q_offset, kl,
+                    softmax_scale, dq=dq, dk=dk[:, lo:hi], dv=dv[:, lo:hi], workspace=ws,
+                    kv_offset=lo, dq_accumulate=(n > 0))
+    return dq, dk, dv

@@ -94,6 +94,9 @@ def _params(**kw):
     (dict(d=256), UNSUPPORTED),
     (dict(causal=2), INVALID),
     (dict(q_offset=-1), INVALID),
+    (dict(kv_offset=-1), INVALID),
+    (dict(dq_accumulate=2), INVALID),
+    (dict(kv_offset=(1 << 30) - 100), UNSUPPORTED),   # kv_offset + sk above 2^30
     (dict(sq=-1), INVALID),
     (dict(B=-2), INVALID),
     (dict(q=None), INVALID),
@@ -134,3 +137,43 @@ def test_empty_problems_launch_nothing(lib):
     for kw in (dict(B=0), dict(H=0), dict(sq=0)):
         p = _params(**kw)
         assert lib.sp_attn_fwd(ctypes.byref(p), FAKE, FAKE, None) == OK
+
+
+def _merge(**kw):
+    p = binding.SpMergeParams()
+    p.B, p.H, p.sq, p.d, p.init = 2, 3, 100, 128, 0
+    p.o_part = p.o_acc = FAKE
+    p.part_stride = (ctypes.c_int64 * 3)(100 * 3 * 128, 3 * 128, 128)
+    p.lse_part = p.lse_acc = FAKE
+    p.o_out = None
+    p.out_stride = (ctypes.c_int64 * 3)(0, 0, 0)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), UNSUPPORTED),
+    (dict(sq=-1), INVALID),
+    (dict(o_part=None), INVALID),
+    (dict(lse_acc=None), INVALID),
+    (dict(o_acc=FAKE_ODD), MISALIGNED),
+    (dict(lse_part=FAKE + 2), MISALIGNED),
+    (dict(part_stride=(ctypes.c_int64 * 3)(4, 4, 4)), MISALIGNED),
+    (dict(o_out=FAKE_ODD), MISALIGNED),
+    (dict(B=0), OK),                                  # nothing to merge, nothing launched
+])
+def test_merge_validation(lib, kw, code):
+    p = _merge(**kw)
+    assert lib.sp_attn_merge(ctypes.byref(p), None) == code
+
+
+def test_merge_null_params(lib):
+    assert lib.sp_attn_merge(None, None) == INVALID
+
+
+def test_noalloc_refuses_dq_accumulation(lib):
+    """The shared scratch carries no accumulation between calls."""
+    p = _params(dq_accumulate=1)
+    assert lib.sp_attn_bwd_noalloc(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   None) == INVALID
