@@ -71,8 +71,10 @@ def relayout_bytes_per_step(w) -> int:
     return 0 if w.N == 1 else 8 * 2 * tensor_bytes(w)
 
 
-def launches_per_step(w) -> int:
+def launches_per_step(w, ring_chunks: int = 0) -> int:
     relayouts = 0 if w.N == 1 else 4
+    if ring_chunks > 1:                   # per chunk: fwd + merge, main + dQ convert;
+        return relayouts + ring_chunks * 4 + 1   # statistics once (later chunks reuse them)
     return relayouts + 1 + 3              # fwd; bwd = statistics + main + dQ convert
 
 
@@ -250,8 +252,9 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w):
-    return {"workload": w.name, "b": w.b, "heads": w.h, "head_dim": w.d, "seq_len": w.s,
+def config_of(w, ring_chunks: int = 0):
+    extra = {"ring_chunks": ring_chunks} if ring_chunks > 1 else {}
+    return {**extra, "workload": w.name, "b": w.b, "heads": w.h, "head_dim": w.d, "seq_len": w.s,
             "sp_degree": w.N, "heads_per_group": w.h_local, "causal": w.causal,
             "input_scale": w.scale,
             "l2": f"inputs larger than L2 ({tensor_bytes(w) / 2**20:.0f} MiB per tensor, 126 MB L2)",
@@ -280,6 +283,21 @@ class EventTimer:
     def mean_ms(self):
         return {n: sum(a.elapsed_time(b) for a, b in ps) / len(ps) for n, ps in self.pairs.items()}
 
+    def per_step_ms(self, steps):
+        return {n: sum(a.elapsed_time(b) for a, b in ps) / steps for n, ps in self.pairs.items()}
+
+
+def merge_bytes_per_step(w, chunks: int) -> int:
+    """sp_attn_merge over `chunks` key chunks: every call reads the bf16 partial (2 B per
+    element) and writes the fp32 accumulator (4 B); all but the first also read it (4 B);
+    the last also writes the bf16 output (2 B); plus 4-byte lse values per row (read the
+    partial's, read and write the accumulator's)."""
+    elems = w.b * w.s * w.h * w.d
+    rows = w.b * w.s * w.h
+    per_elem = 6 + 10 * (chunks - 2) + 12 if chunks > 1 else 8
+    per_row = 8 + 12 * (chunks - 1)
+    return elems * per_elem + rows * per_row
+
 
 def run_ours(args, w):
     world, rank, local = dist_env()
@@ -293,7 +311,7 @@ def run_ours(args, w):
     ins = workloads.make_inputs(w, device=device)
     timer = EventTimer()
     step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=ins["key_len"],
-                            device=device, timer=timer)
+                            device=device, timer=timer, ring_chunks=args.ring)
 
     def one_step():
         step.forward(ins["q"], ins["k"], ins["v"])
@@ -366,14 +384,16 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return 0
 
-    fwd_ms = calls.get("attn_fwd")
-    bwd_ms = calls.get("attn_bwd")
+    per_step = timer.per_step_ms(args.steps)
+    ring = args.ring > 1
+    fwd_ms = per_step.get("ring_chunk_fwd" if ring else "attn_fwd")
+    bwd_ms = per_step.get("ring_chunk_bwd" if ring else "attn_bwd")
     fwd_f = attn_fwd_flops(w)
     peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     bwd_tf = 2.5 * fwd_f / (bwd_ms * 1e-3) / 1e12
-    traffic = recorded_traffic("attn_bwd_llama70b.md", ["attn_bwd.cu", "ptx.cuh"])
+    traffic = None if ring else recorded_traffic("attn_bwd_llama70b.md", ["attn_bwd.cu", "ptx.cuh"])
     relayout_ms = sum(calls.get(n, 0.0) for n in ("seq2head_qkv", "head2seq_o", "seq2head_do",
                                                     "head2seq_grads"))
     relayout = None
@@ -382,12 +402,24 @@ def run_ours(args, w):
         relayout = {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                     "bytes_per_step": relayout_bytes_per_step(w), "ms_per_step": relayout_ms}
     kernels = {}
+    ring_info = None
     for n, ms in calls.items():
         entry = {"ms": ms}
-        if n == "attn_fwd":
-            entry["tflops"] = fwd_f / (ms * 1e-3) / 1e12
-        elif n == "attn_bwd":
-            entry["tflops"] = 2.5 * fwd_f / (ms * 1e-3) / 1e12
+        if n in ("attn_fwd", "ring_chunk_fwd"):
+            entry["ms_per_step"] = per_step[n]
+            entry["tflops"] = fwd_f / (per_step[n] * 1e-3) / 1e12
+        elif n in ("attn_bwd", "ring_chunk_bwd"):
+            entry["ms_per_step"] = per_step[n]
+            entry["tflops"] = 2.5 * fwd_f / (per_step[n] * 1e-3) / 1e12
+        elif n == "ring_merge":
+            entry["ms_per_step"] = per_step[n]
+            nbytes = merge_bytes_per_step(w, args.ring)
+            gbs = nbytes / (per_step[n] * 1e-3) / 1e9
+            entry["gbs"] = gbs
+            ring_info = {"chunks": args.ring,
+                         "merge": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                   "frac": gbs / hbm, "bytes_per_step": nbytes,
+                                   "ms_per_step": per_step[n]}}
         else:
             tensors = 3 if n in ("seq2head_qkv", "head2seq_grads") else 1
             entry["gbs"] = tensors * 2 * tensor_bytes(w) / (ms * 1e-3) / 1e9
@@ -397,18 +429,21 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)*scale bf16, shapes of the workload)",
-        "config": config_of(w),
+        "config": config_of(w, args.ring),
         "pct_bf16_peak": {"burst": value / peak_burst, "sustained": value / peak_sus,
                           "peaks": peak_kind},
-        "roofline": {"kernel": "sp_attn_bwd (statistics + tcgen05 main + dQ convert)",
+        "roofline": {"kernel": (f"sp_attn_bwd over {args.ring} key chunks (statistics + tcgen05 "
+                                "main + dQ convert each)") if ring else
+                               "sp_attn_bwd (statistics + tcgen05 main + dQ convert)",
                      "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
                      "frac": bwd_tf / peak_sus, "peak_kind": f"{peak_kind} sustained bf16",
                      "frac_of_burst": bwd_tf / peak_burst, "traffic": traffic,
                      "algorithmic_flops_per_launch": 2.5 * fwd_f},
         "relayout": relayout,
         "kernels": kernels,
+        "ring": ring_info,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(w) * args.steps,
+        "gpu_launches": launches_per_step(w, args.ring) * args.steps,
         "clocks": clock_summary,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -428,6 +463,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ring", type=int, default=0,
+                    help="run the attention blockwise over this many key chunks (ring attention "
+                         "on one GPU: chunked forward + merge, chunked backward)")
     ap.add_argument("--heads", type=int, default=None,
                     help="total heads instead of the workload's (same sequence, head dim and "
                          "shard count; for profiling a smaller case of the same kernels)")

@@ -148,8 +148,10 @@ size_t sp_attn_bwd_workspace_size(const sp_attn_params* p);
  *              chunk's k, v and kv_offset, and the merged o and lse): this call's dq
  *              contribution is added to the fp32 accumulator the previous call left in
  *              the same workspace (same B, H, sq, d), and dq receives the running sum.
- *              The first chunk's call uses dq_accumulate = 0.  dk and dv are always
- *              this call's (this chunk's) gradients.
+ *              The per-row statistics of that call are reused too, so o, lse and dout
+ *              must be the previous call's.  The first chunk's call uses
+ *              dq_accumulate = 0.  dk and dv are always this call's (this chunk's)
+ *              gradients.
  * Errors as sp_attn_fwd, plus SP_ERR_WORKSPACE when workspace_bytes is too small.
  */
 sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse,

@@ -9,8 +9,8 @@
 // Three launches:
 //   1. bwd_prep: per query row D_i and -lse_i*log2(e) into the workspace (padded
 //      and empty rows get -inf, D = 0 so they contribute nothing), and zero the fp32
-//      dQ accumulator unless the call continues an accumulation over key chunks.
-//      Bandwidth bound.
+//      dQ accumulator.  Skipped by a call that continues an accumulation over key
+//      chunks: its rows, o, lse and dout are the previous call's.  Bandwidth bound.
 //   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
 //      128-row query tiles that can see it (causal: from the diagonal down).  Two
 //      compute warpgroups each own 64 of a tile's query columns.
@@ -555,8 +555,9 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   const int64_t bh = static_cast<int64_t>(g.B) * g.H;
   if (bh == 0 || (g.sq == 0 && g.sk == 0)) return cudaSuccess;
   cudaError_t e;
-  // 1. statistics + zero the dQ accumulator
-  {
+  // 1. statistics + zero the dQ accumulator; a call that continues an accumulation
+  //    over key chunks reuses both (same o, lse and dout as the previous call)
+  if (!a.dq_accumulate) {
     const int64_t warps = bh * rows;
     const int64_t blocks = (warps * 32 + 255) / 256;
     if (blocks > 0) {

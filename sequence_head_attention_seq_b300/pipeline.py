@@ -21,9 +21,11 @@ from .binding import (sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd, sp_a
 class UlyssesAttention:
     def __init__(self, N: int, b: int, s: int, h: int, d: int, causal: bool = True,
                  key_len: torch.Tensor | None = None, softmax_scale: float | None = None,
-                 device="cuda", timer=None):
+                 device="cuda", timer=None, ring_chunks: int = 0):
         """`timer(name)`, if given, returns a context manager wrapped around each
-        library call (used to bracket calls with CUDA events)."""
+        library call (used to bracket calls with CUDA events).  ring_chunks > 1 runs the
+        attention blockwise over that many equal key chunks (ring attention) instead of
+        in one call."""
         if s % N or h % N:
             raise ValueError("s and h must be divisible by N")
         self.N, self.b, self.s, self.h, self.d = N, b, s, h, d
@@ -47,6 +49,13 @@ class UlyssesAttention:
         ws = sp_attn_bwd_workspace_size(self._g(self.qg), self._g(self.kg), self._g(self.vg),
                                         causal, 0, self.key_len, softmax_scale)
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        self.ring_chunks = int(ring_chunks)
+        if self.ring_chunks > 1:
+            if s % self.ring_chunks:
+                raise ValueError("s must be divisible by ring_chunks")
+            c = s // self.ring_chunks
+            self.chunks = [(n * c, (n + 1) * c) for n in range(self.ring_chunks)]
+            self.ring_bufs = {}
 
     def _g(self, t: torch.Tensor) -> torch.Tensor:
         """Group buffer [N][b][s][hl][d] viewed as attention batch [N*b][s][hl][d]."""
@@ -71,15 +80,33 @@ class UlyssesAttention:
     def forward(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> torch.Tensor:
         """q, k, v: [N][b][s/N][h][d] shards -> O shards (same layout)."""
         self._to_groups((q, k, v), (self.qg, self.kg, self.vg), "seq2head_qkv")
-        with self.timer("attn_fwd"):
-            sp_attn_fwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self.causal, 0,
-                        self.key_len, self.softmax_scale, out=self._g(self.og), lse=self.lse)
+        if self.ring_chunks > 1:
+            out, lse, _ = ring_attention_fwd(self._g(self.qg), self._g(self.kg), self._g(self.vg),
+                                             self.chunks, self.causal, 0, self.key_len,
+                                             self.softmax_scale, bufs=self.ring_bufs,
+                                             timer=self.timer)
+            self.og = out.view(self.og.shape)
+            self.lse = lse
+        else:
+            with self.timer("attn_fwd"):
+                sp_attn_fwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self.causal,
+                            0, self.key_len, self.softmax_scale, out=self._g(self.og),
+                            lse=self.lse)
         self._to_shards((self.og,), (self.o,), "head2seq_o")
         return self.o
 
     def backward(self, dout: torch.Tensor):
         """dout shards -> (dq, dk, dv) shards; uses the last forward's O and lse."""
         self._to_groups((dout,), (self.dog,), "seq2head_do")
+        if self.ring_chunks > 1:
+            ring_attention_bwd(self._g(self.qg), self._g(self.kg), self._g(self.vg),
+                               self._g(self.og), self.lse, self._g(self.dog), self.chunks,
+                               self.causal, 0, self.key_len, self.softmax_scale,
+                               dq=self._g(self.dqg), dk=self._g(self.dkg), dv=self._g(self.dvg),
+                               workspace=self.workspace, timer=self.timer)
+            self._to_shards((self.dqg, self.dkg, self.dvg), (self.dq, self.dk, self.dv),
+                            "head2seq_grads")
+            return self.dq, self.dk, self.dv
         with self.timer("attn_bwd"):
             sp_attn_bwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self._g(self.og),
                         self.lse, self._g(self.dog), self.causal, 0, self.key_len,
@@ -98,44 +125,54 @@ def _chunk_key_len(key_len, lo, hi):
 
 
 def ring_attention_fwd(q, k, v, chunks, causal=True, q_offset=0, key_len=None,
-                       softmax_scale=None):
+                       softmax_scale=None, bufs=None, timer=None):
     """Blockwise (ring) attention on one GPU: the keys are visited chunk by chunk, as the
     K/V blocks of a ring arrive at one device ("adv07: Sequence Parallel", sections 5
     and 7), and each chunk's (o, lse) is merged into an fp32 accumulator.
 
     q [B][sq][H][d], k/v [B][sk][H][d]; chunks = [(lo, hi), ...] partitioning [0, sk)
-    in visiting order.  Returns (out bf16, lse fp32, o_acc fp32)."""
+    in visiting order.  Returns (out bf16, lse fp32, o_acc fp32).  `bufs` (a dict, filled
+    on first use) keeps the buffers between calls; `timer(name)` brackets each call."""
     B, sq, H, d = q.shape
-    part = torch.empty_like(q, memory_format=torch.contiguous_format)
-    part_lse = torch.empty((B, H, sq), dtype=torch.float32, device=q.device)
-    o_acc = torch.empty((B, sq, H, d), dtype=torch.float32, device=q.device)
-    lse = torch.empty((B, H, sq), dtype=torch.float32, device=q.device)
-    out = torch.empty_like(part)
+    bufs = {} if bufs is None else bufs
+    if "part" not in bufs:
+        bufs["part"] = torch.empty((B, sq, H, d), dtype=torch.bfloat16, device=q.device)
+        bufs["part_lse"] = torch.empty((B, H, sq), dtype=torch.float32, device=q.device)
+        bufs["o_acc"] = torch.empty((B, sq, H, d), dtype=torch.float32, device=q.device)
+        bufs["lse"] = torch.empty((B, H, sq), dtype=torch.float32, device=q.device)
+        bufs["out"] = torch.empty((B, sq, H, d), dtype=torch.bfloat16, device=q.device)
+    part, part_lse, o_acc, lse, out = (bufs[n] for n in ("part", "part_lse", "o_acc", "lse", "out"))
+    timer = timer if timer is not None else (lambda name: contextlib.nullcontext())
     for n, (lo, hi) in enumerate(chunks):
-        sp_attn_fwd(q, k[:, lo:hi], v[:, lo:hi], causal, q_offset,
-                    _chunk_key_len(key_len, lo, hi), softmax_scale, out=part, lse=part_lse,
-                    kv_offset=lo)
-        sp_attn_merge(part, part_lse, o_acc, lse, init=(n == 0),
-                      o_out=out if n == len(chunks) - 1 else None)
+        with timer("ring_chunk_fwd"):
+            sp_attn_fwd(q, k[:, lo:hi], v[:, lo:hi], causal, q_offset,
+                        _chunk_key_len(key_len, lo, hi), softmax_scale, out=part, lse=part_lse,
+                        kv_offset=lo)
+        with timer("ring_merge"):
+            sp_attn_merge(part, part_lse, o_acc, lse, init=(n == 0),
+                          o_out=out if n == len(chunks) - 1 else None)
     return out, lse, o_acc
 
 
 def ring_attention_bwd(q, k, v, out, lse, dout, chunks, causal=True, q_offset=0, key_len=None,
-                       softmax_scale=None):
+                       softmax_scale=None, dq=None, dk=None, dv=None, workspace=None,
+                       timer=None):
     """Backward of ring_attention_fwd, chunk by chunk with the merged out and lse: each
     chunk's call yields that chunk's dk, dv and adds its dq contribution to an fp32
     accumulator kept in the shared workspace."""
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
-    ws = None
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace
+    timer = timer if timer is not None else (lambda name: contextlib.nullcontext())
     for n, (lo, hi) in enumerate(chunks):
         kl = _chunk_key_len(key_len, lo, hi)
         if ws is None:
             size = sp_attn_bwd_workspace_size(q, k[:, lo:hi], v[:, lo:hi], causal, q_offset, kl,
                                               softmax_scale, kv_offset=lo)
             ws = torch.empty(max(size, 1), dtype=torch.uint8, device=q.device)
-        sp_attn_bwd(q, k[:, lo:hi], v[:, lo:hi], out, lse, dout, causal, q_offset, kl,
-                    softmax_scale, dq=dq, dk=dk[:, lo:hi], dv=dv[:, lo:hi], workspace=ws,
-                    kv_offset=lo, dq_accumulate=(n > 0))
+        with timer("ring_chunk_bwd"):
+            sp_attn_bwd(q, k[:, lo:hi], v[:, lo:hi], out, lse, dout, causal, q_offset, kl,
+                        softmax_scale, dq=dq, dk=dk[:, lo:hi], dv=dv[:, lo:hi], workspace=ws,
+                        kv_offset=lo, dq_accumulate=(n > 0))
     return dq, dk, dv

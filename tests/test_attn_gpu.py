@@ -251,14 +251,15 @@ def _check_tiny_split_q(w, ins):
     check_grad(dvs.double().cpu().numpy(), rdv, "tiny split-Q dv sum")
 
 
-@pytest.mark.parametrize("name", ["llama70b", "ulysses131k"])
-def test_workload_sampled_rows(name):
+@pytest.mark.parametrize("name,ring", [("llama70b", 0), ("ulysses131k", 0), ("llama70b", 8)])
+def test_workload_sampled_rows(name, ring):
     """Long workloads: sampled query rows (out, lse, dq) and the last key rows (dk, dv)
-    of sampled heads against the oracle, plus the gradient-sum properties on every head."""
+    of sampled heads against the oracle, plus the gradient-sum properties on every head.
+    ring > 1: the same step with attention run blockwise over that many key chunks."""
     need_gpu()
     w = workloads.WORKLOADS[name]
     ins = workloads.make_inputs(w, device="cuda")
-    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal)
+    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, ring_chunks=ring)
     step.forward(ins["q"], ins["k"], ins["v"])
     step.backward(ins["dout"])
     torch.cuda.synchronize()
