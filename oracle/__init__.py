@@ -33,7 +33,7 @@ class _Problem(ctypes.Structure):
         ("B", ctypes.c_int), ("H", ctypes.c_int), ("sq", ctypes.c_int),
         ("sk", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int),
         ("q_offset", ctypes.c_int), ("key_len", ctypes.POINTER(ctypes.c_int32)),
-        ("scale", ctypes.c_double),
+        ("key_mask", ctypes.POINTER(ctypes.c_uint8)), ("scale", ctypes.c_double),
     ]
 
 
@@ -105,24 +105,33 @@ def _u16(a) -> np.ndarray:
 class Problem:
     """Shapes and mask of one attention problem (q: [B][sq][H][d], k/v: [B][sk][H][d])."""
 
-    def __init__(self, B, H, sq, sk, d, causal, q_offset=0, key_len=None, scale=None):
+    def __init__(self, B, H, sq, sk, d, causal, q_offset=0, key_len=None, scale=None,
+                 key_mask=None):
         self.B, self.H, self.sq, self.sk, self.d = int(B), int(H), int(sq), int(sk), int(d)
         self.causal = bool(causal)
         self.q_offset = int(q_offset)
         self.key_len = None if key_len is None else np.ascontiguousarray(
             np.asarray(key_len, dtype=np.int32))
+        self.key_mask = None
+        if key_mask is not None:
+            m = np.ascontiguousarray(np.asarray(key_mask) != 0, dtype=np.uint8)
+            if m.shape != (self.B, self.sk):
+                raise ValueError("key_mask must be [B][sk]")
+            self.key_mask = m
         self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
 
     @classmethod
-    def of(cls, q, k, causal, q_offset=0, key_len=None, scale=None) -> "Problem":
+    def of(cls, q, k, causal, q_offset=0, key_len=None, scale=None, key_mask=None) -> "Problem":
         B, sq, H, d = q.shape
-        return cls(B, H, sq, k.shape[1], d, causal, q_offset, key_len, scale)
+        return cls(B, H, sq, k.shape[1], d, causal, q_offset, key_len, scale, key_mask)
 
     def c_struct(self) -> _Problem:
         kl = (self.key_len.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
               if self.key_len is not None else ctypes.POINTER(ctypes.c_int32)())
+        km = (self.key_mask.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+              if self.key_mask is not None else ctypes.POINTER(ctypes.c_uint8)())
         return _Problem(self.B, self.H, self.sq, self.sk, self.d, int(self.causal),
-                        self.q_offset, kl, self.scale)
+                        self.q_offset, kl, km, self.scale)
 
 
 class Oracle:
@@ -138,10 +147,10 @@ class Oracle:
     def threads(self) -> int:
         return int(self.lib.oracle_get_threads())
 
-    def attn_fwd(self, q, k, v, causal, q_offset=0, key_len=None, scale=None):
+    def attn_fwd(self, q, k, v, causal, q_offset=0, key_len=None, scale=None, key_mask=None):
         """out [B][sq][H][d], lse [B][H][sq] (natural log) for all rows."""
         q, k, v = _f64(q), _f64(k), _f64(v)
-        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale, key_mask)
         out = np.empty_like(q)
         lse = np.empty((P.B, P.H, P.sq), dtype=np.float64)
         cp = P.c_struct()
@@ -150,10 +159,11 @@ class Oracle:
             raise ValueError("oracle_attn_fwd rejected the problem")
         return out, lse
 
-    def attn_bwd(self, q, k, v, dout, causal, q_offset=0, key_len=None, scale=None):
+    def attn_bwd(self, q, k, v, dout, causal, q_offset=0, key_len=None, scale=None,
+                 key_mask=None):
         """dq [B][sq][H][d], dk/dv [B][sk][H][d] for all rows."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
-        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale, key_mask)
         dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
         cp = P.c_struct()
         if self.lib.oracle_attn_bwd(ctypes.byref(cp), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
@@ -162,10 +172,10 @@ class Oracle:
         return dq, dk, dv
 
     def attn_fwd_rows(self, q, k, v, b, h, i0, i1, causal, q_offset=0, key_len=None,
-                      scale=None):
+                      scale=None, key_mask=None):
         """out [i1-i0][d], lse [i1-i0] for query rows [i0, i1) of head (b, h)."""
         q, k, v = _f64(q), _f64(k), _f64(v)
-        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale, key_mask)
         out = np.empty((max(i1 - i0, 0) + 1, P.d), dtype=np.float64)
         lse = np.empty((max(i1 - i0, 0) + 1,), dtype=np.float64)
         cp = P.c_struct()
@@ -175,10 +185,10 @@ class Oracle:
         return out[: i1 - i0], lse[: i1 - i0]
 
     def attn_bwd_rows(self, q, k, v, dout, b, h, i0, i1, j0, j1, causal, q_offset=0,
-                      key_len=None, scale=None):
+                      key_len=None, scale=None, key_mask=None):
         """dq rows [i0, i1) and dk/dv rows [j0, j1) of head (b, h)."""
         q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
-        P = Problem.of(q, k, causal, q_offset, key_len, scale)
+        P = Problem.of(q, k, causal, q_offset, key_len, scale, key_mask)
         dq = np.zeros((max(i1 - i0, 0) + 1, P.d), dtype=np.float64)
         dk = np.zeros((max(j1 - j0, 0) + 1, P.d), dtype=np.float64)
         dv = np.zeros((max(j1 - j0, 0) + 1, P.d), dtype=np.float64)

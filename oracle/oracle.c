@@ -26,6 +26,10 @@
  * Readings where the pages are silent (each is listed in the design notes):
  *  - key padding is right padding: key j of batch b is valid iff
  *    j < key_len[b];
+ *  - a general key mask (the transformers PR 31525 collator's
+ *    attention_mask = input_ids != pad_token_id, pads anywhere) removes key j
+ *    of batch b where key_mask[b][j] == 0; it combines with the causal rule
+ *    and key_len (a key must pass all three);
  *  - a row with no valid key has out = 0, lse = -inf and no gradient;
  *  - lse is the natural-log log-sum-exp of the scaled scores;
  *  - the backward pass is the textbook derivative of the forward definition
@@ -56,6 +60,7 @@ typedef struct {
     int causal;            /* 1: key j visible from row i iff j <= q_offset + i */
     int q_offset;          /* global sequence position of query row 0 */
     const int32_t* key_len;/* NULL, or [B]: keys j >= key_len[b] are padding */
+    const uint8_t* key_mask;/* NULL, or [B][sk]: key j of batch b takes part iff nonzero */
     double scale;          /* multiplies q.k; the pages use 1/sqrt(head_dim) */
 } oracle_problem;
 
@@ -77,6 +82,7 @@ static int visible(const oracle_problem* p, int b, int i, int j)
 {
     if (p->causal && j > p->q_offset + i) return 0;
     if (p->key_len != NULL && j >= p->key_len[b]) return 0;
+    if (p->key_mask != NULL && p->key_mask[(size_t)b * p->sk + j] == 0) return 0;
     return 1;
 }
 

@@ -38,7 +38,7 @@ def _bhsd(x):
     return torch.tensor(x, dtype=torch.float64).permute(0, 2, 1, 3).contiguous()
 
 
-def _allowed(B, sq, sk, causal, q_offset, key_len):
+def _allowed(B, sq, sk, causal, q_offset, key_len, key_mask=None):
     """Boolean [B][1][sq][sk]: True where key j takes part for row i."""
     i = torch.arange(sq).view(sq, 1)
     j = torch.arange(sk).view(1, sk)
@@ -48,16 +48,19 @@ def _allowed(B, sq, sk, causal, q_offset, key_len):
     if key_len is not None:
         kl = torch.tensor(np.asarray(key_len), dtype=torch.int64).view(B, 1, 1, 1)
         m &= j.view(1, 1, 1, sk) < kl
+    if key_mask is not None:
+        m &= torch.tensor(np.asarray(key_mask) != 0).view(B, 1, 1, sk)
     return m
 
 
-def _torch_reference(q, k, v, dout, causal, q_offset, key_len, scale):
+def _torch_reference(q, k, v, dout, causal, q_offset, key_len, scale, key_mask=None):
     """torch fp64: out, lse, dq, dk, dv through sdpa + autograd (rows with no key dropped)."""
     B, sq, H, d = q.shape
     sk = k.shape[1]
     tq, tk, tv = (_bhsd(a).requires_grad_() for a in (q, k, v))
-    mask = _allowed(B, sq, sk, causal, q_offset, key_len)
+    mask = _allowed(B, sq, sk, causal, q_offset, key_len, key_mask)
     out = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale)
+    out = torch.nan_to_num(out, nan=0.0)           # rows with no visible key
     scores = torch.matmul(tq, tk.transpose(-1, -2)) * scale
     lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1)
     rows_ok = mask.any(-1, keepdim=True)        # [B][1][sq][1]
@@ -123,6 +126,65 @@ def pin_sdpa_masks(orc):
         _close(dq, r_dq, 1e-11, "dq " + tag)
         _close(dk, r_dk, 1e-11, "dk " + tag)
         _close(dv, r_dv, 1e-11, "dv " + tag)
+
+
+def pin_sdpa_key_mask(orc):
+    """A general key mask (transformers PR 31525 collator: attention_mask = input_ids != pad,
+    pads anywhere), alone and combined with causal, q_offset and key_len: torch fp64 sdpa
+    with the same boolean mask, and its autograd gradients.  One batch entry masks every
+    key (out 0, lse -inf, no gradient)."""
+    B, H, d = 3, 2, 8
+    rng = np.random.default_rng(190)
+    for (sq, sk, causal, q_offset, key_len) in [(21, 37, True, 16, None),
+                                                (30, 30, False, 0, None),
+                                                (19, 44, True, 25, [44, 30, 20])]:
+        mask = rng.random((B, sk)) < 0.7
+        mask[1, :] = False                         # a batch entry with no key at all
+        mask[0, 0] = True
+        q = _rand((B, sq, H, d), 191 + sq)
+        k, v = _rand((B, sk, H, d), 192 + sk), _rand((B, sk, H, d), 193 + sk)
+        do = _rand((B, sq, H, d), 194)
+        scale = 0.4
+        out, lse = orc.attn_fwd(q, k, v, causal, q_offset, key_len, scale, key_mask=mask)
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, causal, q_offset, key_len, scale, key_mask=mask)
+        r_out, r_lse, r_dq, r_dk, r_dv, ok = _torch_reference(q, k, v, do, causal, q_offset,
+                                                              key_len, scale, mask)
+        tag = f"sq={sq} sk={sk} causal={causal} off={q_offset} kl={key_len}"
+        _close(out, r_out, 1e-12, "out " + tag)
+        _close(np.where(ok[:, None, :], lse, 0), np.where(ok[:, None, :], r_lse, 0), 1e-12,
+               "lse " + tag)
+        assert np.all(lse[1] == -np.inf) and not out[1].any() and not dq[1].any()
+        _close(dq, r_dq, 1e-11, "dq " + tag)
+        _close(dk, r_dk, 1e-11, "dk " + tag)
+        _close(dv, r_dv, 1e-11, "dv " + tag)
+
+
+def pin_key_mask_special_cases(orc):
+    """A mask that keeps the first n keys is right padding (key_len = n); all ones is no
+    mask; a mask that drops the first n keys of a non-causal problem is attention on the
+    remaining keys only."""
+    B, H, sq, sk, d = 2, 2, 13, 29, 8
+    q = _rand((B, sq, H, d), 200)
+    k, v = _rand((B, sk, H, d), 201), _rand((B, sk, H, d), 202)
+    do = _rand((B, sq, H, d), 203)
+    key_len = [29, 11]
+    right = np.arange(sk)[None, :] < np.array(key_len)[:, None]
+    for causal in (True, False):
+        a = orc.attn_fwd(q, k, v, causal, 5, key_mask=right)
+        b = orc.attn_fwd(q, k, v, causal, 5, key_len)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b)), "right padding"
+        a = orc.attn_bwd(q, k, v, do, causal, 5, key_mask=right)
+        b = orc.attn_bwd(q, k, v, do, causal, 5, key_len)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b)), "right padding bwd"
+        a = orc.attn_fwd(q, k, v, causal, 5, key_mask=np.ones((B, sk)))
+        b = orc.attn_fwd(q, k, v, causal, 5)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b)), "all-ones mask"
+    n = 9
+    left = np.arange(sk)[None, :].repeat(B, 0) >= n
+    out, lse = orc.attn_fwd(q, k, v, False, key_mask=left)
+    ref, ref_lse = orc.attn_fwd(q, k[:, n:], v[:, n:], False)
+    _close(out, ref, 1e-14, "left padding out")
+    _close(lse, ref_lse, 1e-14, "left padding lse")
 
 
 # ---------------------------------------------------------------- finite differences
@@ -438,4 +500,5 @@ ALL_PINS = [
     pin_key_padding_is_truncation, pin_gradient_sums, pin_empty_rows, pin_rows_api,
     pin_golden_causal_example, pin_golden_split_q, pin_negative_control,
     pin_relayout_golden, pin_relayout_torch, pin_merge_split_kv, pin_merge_closed_forms,
+    pin_sdpa_key_mask, pin_key_mask_special_cases,
 ]

@@ -42,6 +42,12 @@ MUTANTS = {
     "merge_weight_unnormalised": ("const double w = exp(lses[k * lse_part + li] - total);",
                                   "const double w = exp(lses[k * lse_part + li] - m);"),
     "merge_lse_drops_max": ("const double total = m + log(s);", "const double total = log(s);"),
+    "key_mask_ignored": ("if (p->key_mask != NULL && p->key_mask[(size_t)b * p->sk + j] == 0) return 0;",
+                         "if (0) return 0;"),
+    "key_mask_inverted": ("if (p->key_mask != NULL && p->key_mask[(size_t)b * p->sk + j] == 0) return 0;",
+                          "if (p->key_mask != NULL && p->key_mask[(size_t)b * p->sk + j] != 0) return 0;"),
+    "key_mask_batch_stride": ("p->key_mask[(size_t)b * p->sk + j] == 0",
+                              "p->key_mask[(size_t)j] == 0"),
     "head2seq_groups_strided": ("const int g = head / hl, j = head % hl, t = r * sl + u;",
                                 "const int g = head % N, j = head / N, t = r * sl + u;"),
 }
