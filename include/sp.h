@@ -81,7 +81,10 @@ sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int nten
  * from (input_ids != pad).
  *
  * Key j is visible from query row i of batch entry bb iff
- *     (!causal || kv_offset + j <= q_offset + i)  &&  (key_len == NULL || j < key_len[bb]).
+ *     (!causal || kv_offset + j <= q_offset + i)  &&  (key_len == NULL || j < key_len[bb])
+ *     &&  (key_mask == NULL || key_mask[bb * key_mask_stride + j] != 0).
+ * key_mask is a general per-key mask (transformers PR 31525: attention_mask =
+ * input_ids != pad_token_id, pads anywhere); key_len is the right-padding special case.
  * q_offset and kv_offset are the global sequence positions of query row 0 and key
  * row 0: a query shard (split-Q) sets q_offset, a key chunk of ring / blockwise
  * attention sets kv_offset ("adv07: Sequence Parallel", sections 5 and 7: K/V blocks
@@ -109,6 +112,10 @@ typedef struct sp_attn_params {
     const int32_t* key_len;   /* NULL, or DEVICE [B] valid-key counts in [0, sk] */
     float softmax_scale;      /* <= 0 selects 1/sqrt(d) */
     int dq_accumulate;        /* sp_attn_bwd only, 0 or 1: see sp_attn_bwd */
+    const uint8_t* key_mask;  /* NULL, or DEVICE bytes [B][key_mask_stride]: key j of batch
+                                 entry bb takes part iff key_mask[bb*stride + j] != 0;
+                                 16-byte aligned */
+    int64_t key_mask_stride;  /* bytes between batch rows: a multiple of 16, >= sk */
 } sp_attn_params;
 
 /*
@@ -120,9 +127,10 @@ typedef struct sp_attn_params {
  * lse : DEVICE fp32 [B][H][sq], contiguous.  Needed by sp_attn_bwd.
  * Errors: B, H, sq, sk < 0, q_offset < 0, kv_offset < 0, causal not 0/1, NULL
  *         pointers -> SP_ERR_INVALID_ARG (B, H, sq or sk equal to 0 is allowed:
- *         nothing to do, SP_OK); d not 64/128, q_offset + sq or kv_offset + sk
- *         above 2^30 -> SP_ERR_UNSUPPORTED; pointer/stride alignment ->
- *         SP_ERR_MISALIGNED.
+ *         nothing to do, SP_OK); key_mask_stride < sk with a key_mask ->
+ *         SP_ERR_INVALID_ARG; d not 64/128, q_offset + sq or kv_offset + sk above
+ *         2^30 -> SP_ERR_UNSUPPORTED; pointer/stride alignment (key_mask and its
+ *         stride included) -> SP_ERR_MISALIGNED.
  */
 sp_status sp_attn_fwd(const sp_attn_params* p, void* o, float* lse, void* stream);
 

@@ -50,6 +50,7 @@ class SpAttnParams(ctypes.Structure):
         ("kv_offset", ctypes.c_int),
         ("key_len", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
         ("dq_accumulate", ctypes.c_int),
+        ("key_mask", ctypes.c_void_p), ("key_mask_stride", ctypes.c_int64),
     ]
 
 
@@ -191,8 +192,27 @@ def _strides(t: torch.Tensor, name: str):
     return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
 
 
+def _mask_rows(key_mask, B: int, sk: int):
+    """key_mask as device bytes in rows of a 16-byte-multiple stride (padded copy if needed)."""
+    if not isinstance(key_mask, torch.Tensor) or not key_mask.is_cuda:
+        raise ValueError("key_mask must be a CUDA tensor")
+    if tuple(key_mask.shape) != (B, sk):
+        raise ValueError(f"key_mask must be [B][sk] = [{B}][{sk}]")
+    m = key_mask.to(torch.uint8) if key_mask.dtype == torch.bool else key_mask
+    if m.dtype != torch.uint8:
+        raise ValueError("key_mask must be bool or uint8")
+    ok = (m.stride(1) == 1 and m.stride(0) % 16 == 0 and m.stride(0) >= sk
+          and m.data_ptr() % 16 == 0)
+    if not ok:
+        stride = (sk + 15) // 16 * 16
+        padded = torch.zeros((B, max(stride, 16)), dtype=torch.uint8, device=m.device)
+        padded[:, :sk] = m
+        m = padded
+    return m
+
+
 def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
-                softmax_scale=None, kv_offset: int = 0) -> SpAttnParams:
+                softmax_scale=None, kv_offset: int = 0, key_mask=None) -> SpAttnParams:
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need_bf16_cuda(name, t)
     B, sq, H, d = q.shape
@@ -215,11 +235,19 @@ def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
     else:
         p.key_len = None
     p.softmax_scale = float(softmax_scale) if softmax_scale is not None else 0.0
+    if key_mask is not None:
+        m = _mask_rows(key_mask, B, k.shape[1])
+        p.key_mask = m.data_ptr()
+        p.key_mask_stride = m.stride(0)
+        p._keep = m                     # keeps a padded copy alive while p is in use
+    else:
+        p.key_mask = None
+        p.key_mask_stride = 0
     return p
 
 
 def sp_attn_fwd(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
-                softmax_scale=None, out=None, lse=None, kv_offset: int = 0):
+                softmax_scale=None, out=None, lse=None, kv_offset: int = 0, key_mask=None):
     """out [B][sq][H][d] bf16 and lse [B][H][sq] fp32 (natural log)."""
     lib = load()
     B, sq, H, d = q.shape
@@ -230,22 +258,22 @@ def sp_attn_fwd(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
     _need_bf16_cuda("out", out)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, sq):
         raise ValueError("lse must be contiguous fp32 [B][H][sq]")
-    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset)
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset, key_mask)
     rc = lib.sp_attn_fwd(ctypes.byref(p), out.data_ptr(), lse.data_ptr(), _stream(q.device))
     _check("sp_attn_fwd", rc)
     return out, lse
 
 
 def sp_attn_bwd_workspace_size(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
-                               softmax_scale=None, kv_offset: int = 0) -> int:
+                               softmax_scale=None, kv_offset: int = 0, key_mask=None) -> int:
     lib = load()
-    p = make_params(q, k, v, q, causal, q_offset, key_len, softmax_scale, kv_offset)
+    p = make_params(q, k, v, q, causal, q_offset, key_len, softmax_scale, kv_offset, key_mask)
     return int(lib.sp_attn_bwd_workspace_size(ctypes.byref(p)))
 
 
 def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0, key_len=None,
                 softmax_scale=None, dq=None, dk=None, dv=None, workspace=None,
-                kv_offset: int = 0, dq_accumulate: bool = False):
+                kv_offset: int = 0, dq_accumulate: bool = False, key_mask=None):
     """dq, dk, dv (bf16, layouts of q, k, v) from the forward's out/lse and dout.
 
     Ring / blockwise attention: call once per key chunk (k, v of the chunk, its
@@ -256,7 +284,7 @@ def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
     _need_bf16_cuda("dout", dout)
     if out.shape != dout.shape or not _same_layout(out, dout):
         raise ValueError("out and dout must share shape and strides")
-    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset)
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset, key_mask)
     p.dq_accumulate = 1 if dq_accumulate else 0
 
     def like(t):
@@ -283,7 +311,7 @@ def sp_attn_bwd(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
 
 def sp_attn_bwd_noalloc(q, k, v, out, lse, dout, causal: bool = True, q_offset: int = 0,
                         key_len=None, softmax_scale=None, dq=None, dk=None, dv=None,
-                        kv_offset: int = 0):
+                        kv_offset: int = 0, key_mask=None):
     """sp_attn_bwd with the library's own fixed device scratch instead of a workspace.
 
     For callers that must not allocate device memory during the call: the C entry
@@ -297,7 +325,7 @@ def sp_attn_bwd_noalloc(q, k, v, out, lse, dout, causal: bool = True, q_offset: 
     _need_bf16_cuda("dout", dout)
     if out.shape != dout.shape or not _same_layout(out, dout):
         raise ValueError("out and dout must share shape and strides")
-    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset)
+    p = make_params(q, k, v, out, causal, q_offset, key_len, softmax_scale, kv_offset, key_mask)
 
     def like(t):
         return torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=t.device)

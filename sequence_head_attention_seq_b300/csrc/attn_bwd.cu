@@ -214,7 +214,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const int kvlen = kv_limit(g, b);
   const int m_start = g.causal ? max(0, kv0 - g.q_offset) / kRows : 0;
   const int m_end = (g.sq + kRows - 1) / kRows;
-  const int nq = (kv0 < kvlen) ? max(0, m_end - m_start) : 0;
+  // key mask: does the block hold a masked key below kvlen, and a visible one at all?
+  // (every thread computes the same answer from the same 128 bytes)
+  bool block_masked = false, block_visible = kv0 < kvlen;
+  if (g.key_mask != nullptr && kv0 < kvlen) {
+    const uint8_t* mask_row = g.key_mask + b * g.key_mask_stride;
+    uint32_t masked = 0, visible = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 z = key_mask_zero16(mask_row, kv0 + 16 * u, g.sk);
+      const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t valid = key_lanes_below(kv0 + 16 * u + 4 * w, kvlen);
+        masked |= zw[w] & valid;
+        visible |= ~zw[w] & valid;
+      }
+    }
+    block_masked = masked != 0;
+    block_visible = visible != 0;
+  }
+  // a block with no visible key has zero dK, dV and adds nothing to dQ
+  const int nq = block_visible ? max(0, m_end - m_start) : 0;
 
   if (threadIdx.x == 0) {
     if ((smem_u32(smem_raw) & 1023u) != 0) raise_status(p.status, kStatusBadSmem);
@@ -366,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const uint32_t dp_col = kColDP + wg * kHalf;
     uint8_t* ds_row = sm.ds + wg * 16384 + jj * 128; // row jj of this half's dS chunk
     const int swz = jj & 7;
-    const bool key_ok = key < kvlen;
+    const bool key_ok = key < kvlen && (g.key_mask == nullptr ||
+                                        g.key_mask[b * g.key_mask_stride + key] != 0);
     bool ok = true;
     for (int it = 0; it < nq; ++it) {
       const int s = it & 1;
@@ -384,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const float* nlse2 = sm.stats[s][0] + wg * kHalf;   // -lse * log2(e)
       const float* Dv = sm.stats[s][1] + wg * kHalf;
       const int qh0 = q0 + wg * kHalf;               // first query row of this half
-      const bool need_mask = (kv0 + kKeys > kvlen) ||
+      const bool need_mask = block_masked || (kv0 + kKeys > kvlen) ||
                              (g.causal && kv0 + kKeys - 1 > g.q_offset + qh0);
       // first query column (relative to the half) that sees this key under the causal mask
       const int first_q = g.causal ? key - g.q_offset - qh0 : -(1 << 30);

@@ -241,13 +241,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int c = 0; c < 64; ++c) sv[h2 * 64 + c] = __uint_as_float(raw[c / 32][c % 32]);
       }
       const int key0 = j * kKeys;
-      const bool need_mask = (key0 + kKeys > kvlen) ||
-                             (g.causal && key0 + kKeys - 1 > g.q_offset + tile.q0);
+      bool need_mask = (key0 + kKeys > kvlen) ||
+                       (g.causal && key0 + kKeys - 1 > g.q_offset + tile.q0);
+      const uint8_t* mask_row = g.key_mask != nullptr ? g.key_mask + b * g.key_mask_stride
+                                                      : nullptr;
+      if (mask_row != nullptr && !need_mask) {
+        // a block whose keys all pass the key mask needs no element-wise masking
+        uint32_t any = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 z = key_mask_zero16(mask_row, key0 + 16 * u, g.sk);
+          any |= z.x | z.y | z.z | z.w;
+        }
+        need_mask = any != 0;
+      }
       if (need_mask) {
         const int lim = g.causal ? min(kvlen, gq + 1) : kvlen;   // visible keys: key < lim
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c)
-          if (key0 + c >= lim) sv[c] = -INFINITY;
+        for (int u = 0; u < 8; ++u) {
+          uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          if (mask_row != nullptr) z = key_mask_zero16(mask_row, key0 + 16 * u, g.sk);
+          const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = 16 * u + e;
+            if (key0 + c >= lim || ((zw[e / 4] >> (8 * (e % 4))) & 1u)) sv[c] = -INFINITY;
+          }
+        }
       }
       // row maximum over eight independent chains (a single chain is 127 dependent steps)
       float mx8[8];

@@ -20,6 +20,8 @@ struct AttnGeom {
   int causal;
   int q_offset;               // query row 0's position relative to key row 0 (may be < 0)
   const int32_t* key_len;     // device, may be null
+  const uint8_t* key_mask;    // device [B][key_mask_stride] bytes, may be null
+  int64_t key_mask_stride;
   float scale;                // softmax scale
   float scale_log2;           // scale * log2(e)
 };

@@ -314,6 +314,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// ---------------------------------------------------------------- key mask
+
+// 16 key-mask bytes of one row starting at key `k0` (a multiple of 16), as zero-byte
+// flags: byte b of the result word w is 0xFF where key k0 + 4w + b is masked.  Vectors
+// starting at or past `sk` are not loaded and read as masked; a row holds its stride
+// (a multiple of 16, >= sk) bytes, so no load leaves it.  Bytes at or past sk inside
+// the last vector are row padding: callers also mask keys past the valid length.
+__device__ __forceinline__ uint4 key_mask_zero16(const uint8_t* row, int k0, int sk) {
+  uint4 x = make_uint4(0u, 0u, 0u, 0u);
+  if (k0 < sk) x = __ldg(reinterpret_cast<const uint4*>(row + k0));
+  return make_uint4(__vcmpeq4(x.x, 0u), __vcmpeq4(x.y, 0u), __vcmpeq4(x.z, 0u),
+                    __vcmpeq4(x.w, 0u));
+}
+
+// Byte lanes of a 4-key word that hold keys below `limit` (0xFF per such key).
+__device__ __forceinline__ uint32_t key_lanes_below(int key_of_byte0, int limit) {
+  const int n = limit - key_of_byte0;
+  return n >= 4 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << (8 * n)) - 1u));
+}
+
 // ---------------------------------------------------------------- packed fp32 pairs
 // sm_100-family f32x2 arithmetic: one instruction operates on two fp32 lanes held in a
 // 64-bit register pair (x in the low half), halving the issue slots of elementwise math.

@@ -99,6 +99,10 @@ sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
       !strides_ok(p->o_stride))
     return SP_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(p->key_len) & 3u) != 0) return SP_ERR_MISALIGNED;
+  if (p->key_mask != nullptr) {
+    if (!aligned16(p->key_mask) || p->key_mask_stride % 16 != 0) return SP_ERR_MISALIGNED;
+    if (p->key_mask_stride < p->sk) return SP_ERR_INVALID_ARG;
+  }
   g->B = p->B;
   g->H = p->H;
   g->sq = p->sq;
@@ -109,6 +113,8 @@ sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
   // query rows before a key chunk's start see none of its keys)
   g->q_offset = p->q_offset - p->kv_offset;
   g->key_len = p->key_len;
+  g->key_mask = p->key_mask;
+  g->key_mask_stride = p->key_mask != nullptr ? p->key_mask_stride : 0;
   float scale = p->softmax_scale;
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(p->d));
   g->scale = scale;

@@ -96,6 +96,9 @@ def _params(**kw):
     (dict(q_offset=-1), INVALID),
     (dict(kv_offset=-1), INVALID),
     (dict(dq_accumulate=2), INVALID),
+    (dict(key_mask=FAKE_ODD, key_mask_stride=256), MISALIGNED),
+    (dict(key_mask=FAKE, key_mask_stride=264), MISALIGNED),     # stride not a multiple of 16
+    (dict(key_mask=FAKE, key_mask_stride=240), INVALID),        # stride < sk
     (dict(kv_offset=(1 << 30) - 100), UNSUPPORTED),   # kv_offset + sk above 2^30
     (dict(sq=-1), INVALID),
     (dict(B=-2), INVALID),
