@@ -310,8 +310,15 @@ def run_ours(args, w):
     peaks, peak_kind = load_peaks()
     ins = workloads.make_inputs(w, device=device)
     timer = EventTimer()
-    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=ins["key_len"],
-                            device=device, timer=timer, ring_chunks=args.ring)
+    key_len, key_mask = ins["key_len"], None
+    if args.key_mask:
+        if key_len is None:
+            raise SystemExit("--key-mask needs a workload with padded keys")
+        # the same right padding, expressed as a general per-key mask
+        key_mask = torch.arange(w.s)[None, :] < key_len[:, None]
+        key_len = None
+    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=key_len,
+                            device=device, timer=timer, ring_chunks=args.ring, key_mask=key_mask)
 
     def one_step():
         step.forward(ins["q"], ins["k"], ins["v"])
@@ -429,7 +436,9 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)*scale bf16, shapes of the workload)",
-        "config": config_of(w, args.ring),
+        "config": {**config_of(w, args.ring),
+                   **({"key_mask": "right padding given as a general per-key mask"}
+                      if args.key_mask else {})},
         "pct_bf16_peak": {"burst": value / peak_burst, "sustained": value / peak_sus,
                           "peaks": peak_kind},
         "roofline": {"kernel": (f"sp_attn_bwd over {args.ring} key chunks (statistics + tcgen05 "
@@ -466,6 +475,9 @@ def main(argv=None):
     ap.add_argument("--ring", type=int, default=0,
                     help="run the attention blockwise over this many key chunks (ring attention "
                          "on one GPU: chunked forward + merge, chunked backward)")
+    ap.add_argument("--key-mask", action="store_true",
+                    help="give the workload's key padding as a general per-key mask "
+                         "(the mask path of the kernels) instead of key lengths")
     ap.add_argument("--heads", type=int, default=None,
                     help="total heads instead of the workload's (same sequence, head dim and "
                          "shard count; for profiling a smaller case of the same kernels)")

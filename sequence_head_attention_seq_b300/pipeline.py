@@ -21,11 +21,13 @@ from .binding import (sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd, sp_a
 class UlyssesAttention:
     def __init__(self, N: int, b: int, s: int, h: int, d: int, causal: bool = True,
                  key_len: torch.Tensor | None = None, softmax_scale: float | None = None,
-                 device="cuda", timer=None, ring_chunks: int = 0):
+                 device="cuda", timer=None, ring_chunks: int = 0,
+                 key_mask: torch.Tensor | None = None):
         """`timer(name)`, if given, returns a context manager wrapped around each
         library call (used to bracket calls with CUDA events).  ring_chunks > 1 runs the
         attention blockwise over that many equal key chunks (ring attention) instead of
-        in one call."""
+        in one call.  key_mask ([b][s] bool, True = key takes part) is a general key mask
+        per batch row, applied in every head group."""
         if s % N or h % N:
             raise ValueError("s and h must be divisible by N")
         self.N, self.b, self.s, self.h, self.d = N, b, s, h, d
@@ -38,6 +40,7 @@ class UlyssesAttention:
         bf = dict(dtype=torch.bfloat16, device=dev)
         # key lengths per batch row, repeated for every head group (batch entry g*b + bb)
         self.key_len = None if key_len is None else key_len.to(dev, torch.int32).repeat(N)
+        self.key_mask = None if key_mask is None else key_mask.to(dev).repeat(N, 1)
         self.qg, self.kg, self.vg = (torch.empty(gshape, **bf) for _ in range(3))
         self.og = torch.empty(gshape, **bf)
         self.dog = torch.empty(gshape, **bf)
@@ -50,6 +53,8 @@ class UlyssesAttention:
                                         causal, 0, self.key_len, softmax_scale)
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         self.ring_chunks = int(ring_chunks)
+        if self.ring_chunks > 1 and key_mask is not None:
+            raise ValueError("ring attention here takes key_len, not a general key mask")
         if self.ring_chunks > 1:
             if s % self.ring_chunks:
                 raise ValueError("s must be divisible by ring_chunks")
@@ -91,7 +96,7 @@ class UlyssesAttention:
             with self.timer("attn_fwd"):
                 sp_attn_fwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self.causal,
                             0, self.key_len, self.softmax_scale, out=self._g(self.og),
-                            lse=self.lse)
+                            lse=self.lse, key_mask=self.key_mask)
         self._to_shards((self.og,), (self.o,), "head2seq_o")
         return self.o
 
@@ -111,7 +116,7 @@ class UlyssesAttention:
             sp_attn_bwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self._g(self.og),
                         self.lse, self._g(self.dog), self.causal, 0, self.key_len,
                         self.softmax_scale, dq=self._g(self.dqg), dk=self._g(self.dkg),
-                        dv=self._g(self.dvg), workspace=self.workspace)
+                        dv=self._g(self.dvg), workspace=self.workspace, key_mask=self.key_mask)
         self._to_shards((self.dqg, self.dkg, self.dvg), (self.dq, self.dk, self.dv),
                         "head2seq_grads")
         return self.dq, self.dk, self.dv
