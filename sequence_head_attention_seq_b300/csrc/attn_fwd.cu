@@ -32,6 +32,10 @@ constexpr int kKeys = 128;      // keys per KV block
 constexpr int kStages = 2;
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// With a key mask, key blocks whose keys are all masked are skipped; visibility of the
+// first kVisBlocks blocks (4M keys) is kept as a bitmap, later blocks are never skipped.
+constexpr int kVisWords = 1024;
+constexpr int kVisBlocks = kVisWords * 32;
 
 template <int D>
 struct FwdSmem {
@@ -42,6 +46,7 @@ struct FwdSmem {
   uint64_t q_full;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full, drain;
+  uint32_t vis[kVisWords];      // bit j: key block j has a key the key mask lets through
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -76,7 +81,9 @@ __device__ __forceinline__ TileInfo tile_info(const AttnGeom& g, int kvlen, int 
   return t;
 }
 
-template <int D>
+// kKeyMask: the problem has a general key mask (a separate instantiation, so that the
+// common case carries none of the block-skipping bookkeeping).
+template <int D, bool kKeyMask>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdKernelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(smem_raw);
@@ -117,7 +124,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
+  // key mask: which key blocks hold a visible key (all threads share the loads)
+  constexpr bool use_vis = kKeyMask;
+  const int nvis = min(nmax, kVisBlocks);
+  if constexpr (use_vis)
+    for (int w = threadIdx.x; w < (nvis + 31) / 32; w += blockDim.x) sm.vis[w] = 0u;
   __syncthreads();
+  if constexpr (use_vis) {
+    const uint8_t* mask_row = g.key_mask + b * g.key_mask_stride;
+    for (int j = threadIdx.x; j < nvis; j += blockDim.x) {
+      uint32_t visible = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 z = key_mask_zero16(mask_row, j * kKeys + 16 * u, g.sk);
+        const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          visible |= ~zw[w] & key_lanes_below(j * kKeys + 16 * u + 4 * w, kvlen);
+      }
+      if (visible != 0u) atomicOr(&sm.vis[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+  }
+  // the next key block at or after j that is not skipped (nmax when none is left)
+  auto next_vis = [&](int j) -> int {
+    if constexpr (!use_vis) return j;
+    while (j < nmax) {
+      if (j >= kVisBlocks) return j;
+      const uint32_t w = sm.vis[j >> 5] >> (j & 31);
+      if (w != 0u) return min(j + __ffs(static_cast<int>(w)) - 1, nmax);
+      j = (j | 31) + 1;
+    }
+    return nmax;
+  };
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
@@ -132,9 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     for (int t = 0; t < ntiles; ++t)
       for (int c = 0; c < kChunks; ++c)
         tma_load_4d(sm.q[t] + c * 16384, &p.tq, &sm.q_full, c * 64, h, ti[t].q0, b);
-    for (int j = 0; j < nmax; ++j) {
-      const int s = j % kStages;
-      if (j >= kStages && !mbar_wait(&sm.kv_empty[s], ((j / kStages) - 1) & 1, p.status, abort_flag))
+    // n counts the key blocks visited (stages and phases follow it)
+    for (int j = next_vis(0), n = 0; j < nmax; j = next_vis(j + 1), ++n) {
+      const int s = n % kStages;
+      if (n >= kStages && !mbar_wait(&sm.kv_empty[s], ((n / kStages) - 1) & 1, p.status, abort_flag))
         break;
       mbar_expect_tx(&sm.k_full[s], kTileBytes);
       for (int c = 0; c < kChunks; ++c)
@@ -148,17 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     constexpr uint32_t kIdS = idesc_bf16(kRows, kKeys, false, false);
     constexpr uint32_t kIdO = idesc_bf16(kRows, D, false, true);
     const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
-    int k_ready = -1;   // highest KV block whose K tile has been waited for
+    int k_ready = -1;   // visited KV blocks whose K tile has been waited for
     bool ok = mbar_wait(&sm.q_full, 0, p.status, abort_flag);
-    auto ensure_k = [&](int j) -> bool {
-      if (k_ready >= j) return true;
-      k_ready = j;
-      const bool r = mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, p.status, abort_flag);
+    // n: index of a key block among the visited ones (its ring stage and phase)
+    auto ensure_k = [&](int n) -> bool {
+      if (k_ready >= n) return true;
+      k_ready = n;
+      const bool r = mbar_wait(&sm.k_full[n % kStages], (n / kStages) & 1, p.status, abort_flag);
       tc_fence_after();
       return r;
     };
-    auto issue_s = [&](int t, int j) {
-      const uint32_t k_addr = smem_u32(sm.k[j % kStages]);
+    auto issue_s = [&](int t, int n) {
+      const uint32_t k_addr = smem_u32(sm.k[n % kStages]);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -167,44 +208,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       mma_commit(&sm.s_full[t]);
     };
-    auto issue_pv = [&](int t, int j) {
-      const uint32_t v_addr = smem_u32(sm.v[j % kStages]);
+    auto issue_pv = [&](int t, int n) {
+      const uint32_t v_addr = smem_u32(sm.v[n % kStages]);
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk)
         mma_ts(tmem + kOCol0 + t * D, tmem + t * kKeys + kk * 8,
-               sdesc_sw128(v_addr + kk * 2048, 16384, 1024), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+               sdesc_sw128(v_addr + kk * 2048, 16384, 1024), kIdO, (n > 0 || kk > 0) ? 1u : 0u);
     };
-    if (ok) {
+    const int j0 = next_vis(0);
+    if (ok && j0 < nmax) {
       tc_fence_after();
       ok = ensure_k(0);
       for (int t = 0; t < 2 && ok; ++t)
-        if (ti[t].nblocks > 0) issue_s(t, 0);
+        if (j0 < ti[t].nblocks) issue_s(t, 0);
     }
-    for (int j = 0; j < nmax && ok; ++j) {
-      const int s = j % kStages;
-      if (!(ok = mbar_wait(&sm.v_full[s], (j / kStages) & 1, p.status, abort_flag))) break;
+    for (int j = j0, n = 0; j < nmax && ok; ++n) {
+      const int jn = next_vis(j + 1);   // the next visited block
+      const int s = n % kStages;
+      if (!(ok = mbar_wait(&sm.v_full[s], (n / kStages) & 1, p.status, abort_flag))) break;
       tc_fence_after();
       // tile 0
       if (j < ti[0].nblocks) {
-        if (!(ok = mbar_wait(&sm.p_full[0], j & 1, p.status, abort_flag))) break;
+        if (!(ok = mbar_wait(&sm.p_full[0], n & 1, p.status, abort_flag))) break;
         tc_fence_after();
-        issue_pv(0, j);
+        issue_pv(0, n);
       }
-      if (j + 1 < ti[0].nblocks) {
-        if (!(ok = ensure_k(j + 1))) break;
-        issue_s(0, j + 1);
+      if (jn < ti[0].nblocks) {
+        if (!(ok = ensure_k(n + 1))) break;
+        issue_s(0, n + 1);
       }
       // tile 1
       if (j < ti[1].nblocks) {
-        if (!(ok = mbar_wait(&sm.p_full[1], j & 1, p.status, abort_flag))) break;
+        if (!(ok = mbar_wait(&sm.p_full[1], n & 1, p.status, abort_flag))) break;
         tc_fence_after();
-        issue_pv(1, j);
+        issue_pv(1, n);
       }
       mma_commit(&sm.kv_empty[s]);
-      if (j + 1 < ti[1].nblocks) {
-        if (!(ok = ensure_k(j + 1))) break;
-        issue_s(1, j + 1);
+      if (jn < ti[1].nblocks) {
+        if (!(ok = ensure_k(n + 1))) break;
+        issue_s(1, n + 1);
       }
+      j = jn;
     }
     mma_commit(&sm.o_full);
     if (!ok) {
@@ -226,8 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int gq = g.q_offset + qrow;                // position relative to key row 0
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
-    for (int j = 0; j < tile.nblocks; ++j) {
-      if (!(ok = mbar_wait(&sm.s_full[t], j & 1, p.status, abort_flag))) break;
+    int visited = 0;   // key blocks of this tile that were computed (skipped ones excluded)
+    for (int j = next_vis(0); j < tile.nblocks; j = next_vis(j + 1), ++visited) {
+      const int n = visited;
+      if (!(ok = mbar_wait(&sm.s_full[t], n & 1, p.status, abort_flag))) break;
       tc_fence_after();
       // the score row in two round trips to TMEM of 64 columns each
       float sv[kKeys];
@@ -243,9 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const int key0 = j * kKeys;
       bool need_mask = (key0 + kKeys > kvlen) ||
                        (g.causal && key0 + kKeys - 1 > g.q_offset + tile.q0);
-      const uint8_t* mask_row = g.key_mask != nullptr ? g.key_mask + b * g.key_mask_stride
-                                                      : nullptr;
-      if (mask_row != nullptr && !need_mask) {
+      const uint8_t* mask_row = kKeyMask ? g.key_mask + b * g.key_mask_stride : nullptr;
+      if (kKeyMask && !need_mask) {
         // a block whose keys all pass the key mask needs no element-wise masking
         uint32_t any = 0;
 #pragma unroll
@@ -260,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          if (mask_row != nullptr) z = key_mask_zero16(mask_row, key0 + 16 * u, g.sk);
+          if constexpr (kKeyMask) z = key_mask_zero16(mask_row, key0 + 16 * u, g.sk);
           const uint32_t zw[4] = {z.x, z.y, z.z, z.w};
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -282,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       float m_use = m;
       float alpha = 1.0f;
       bool rescale = false;
-      if (j == 0) {
+      if (n == 0) {
         m_use = m_blk;
       } else if (m_blk > m + kRescaleThreshold) {
         m_use = m_blk;
@@ -305,10 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       l *= alpha;
       m = m_use;
       // P = exp2(S * scale * log2(e) - m), two columns per instruction; the row sum
-      // goes into two independent pair accumulators
-      const uint64_t sc2 = f2_pack(g.scale_log2, g.scale_log2);
-      // a row that sees no key of this tile so far keeps m = -inf; its P must be 0
+      // goes into two independent pair accumulators.  A row that sees no key of this
+      // tile so far keeps m = -inf; its P must be 0.
       const float nm = (m == -INFINITY) ? 0.0f : -m;
+      const uint64_t sc2 = f2_pack(g.scale_log2, g.scale_log2);
       const uint64_t nm2 = f2_pack(nm, nm);
       uint64_t lsum[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
@@ -339,14 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       __nv_bfloat16* orow = p.o + b * p.o_stride[0] + static_cast<int64_t>(qrow) * p.o_stride[1] +
                             h * p.o_stride[2];
       float* lse_out = p.lse + (static_cast<int64_t>(b) * g.H + h) * g.sq + qrow;
-      if (tile.nblocks == 0 || !ok) {
+      if (visited == 0 || !ok) {
         uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
         *lse_out = -INFINITY;
       }
     }
-    if (tile.nblocks > 0 && ok) {
+    if (visited > 0 && ok) {
       ok = mbar_wait(&sm.o_full, 0, p.status, abort_flag);
       tc_fence_after();
       const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
@@ -399,19 +444,21 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   const int64_t nblocks = static_cast<int64_t>(p.num_pairs) * a.g.B * a.g.H;
   if (nblocks == 0) return cudaSuccess;
   if (nblocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  if (a.g.d == 128) {
-    const size_t smem = sizeof(FwdSmem<128>);
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto launch = [&](auto kernel, size_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attn_fwd_kernel<128><<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(p);
-  } else {
-    const size_t smem = sizeof(FwdSmem<64>);
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attn_fwd_kernel<64><<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(p);
-  }
+    kernel<<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(p);
+    return cudaSuccess;
+  };
+  const bool masked = a.g.key_mask != nullptr;
+  cudaError_t e;
+  if (a.g.d == 128)
+    e = masked ? launch(attn_fwd_kernel<128, true>, sizeof(FwdSmem<128>))
+               : launch(attn_fwd_kernel<128, false>, sizeof(FwdSmem<128>));
+  else
+    e = masked ? launch(attn_fwd_kernel<64, true>, sizeof(FwdSmem<64>))
+               : launch(attn_fwd_kernel<64, false>, sizeof(FwdSmem<64>));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
