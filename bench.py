@@ -71,8 +71,8 @@ def relayout_bytes_per_step(w) -> int:
     return 0 if w.N == 1 else 8 * 2 * tensor_bytes(w)
 
 
-def launches_per_step(w, ring_chunks: int = 0) -> int:
-    relayouts = 0 if w.N == 1 else 4
+def launches_per_step(w, ring_chunks: int = 0, fused: bool = False) -> int:
+    relayouts = 0 if (w.N == 1 or fused) else 4
     if ring_chunks > 1:                   # per chunk: fwd + merge, main + dQ convert;
         return relayouts + ring_chunks * 4 + 1   # statistics once (later chunks reuse them)
     return relayouts + 1 + 3              # fwd; bwd = statistics + main + dQ convert
@@ -318,7 +318,8 @@ def run_ours(args, w):
         key_mask = torch.arange(w.s)[None, :] < key_len[:, None]
         key_len = None
     step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=key_len,
-                            device=device, timer=timer, ring_chunks=args.ring, key_mask=key_mask)
+                            device=device, timer=timer, ring_chunks=args.ring, key_mask=key_mask,
+                            fused=args.fused)
 
     def one_step():
         step.forward(ins["q"], ins["k"], ins["v"])
@@ -438,7 +439,8 @@ def run_ours(args, w):
         "data": "synthetic (seeded N(0,1)*scale bf16, shapes of the workload)",
         "config": {**config_of(w, args.ring),
                    **({"key_mask": "right padding given as a general per-key mask"}
-                      if args.key_mask else {})},
+                      if args.key_mask else {}),
+                   **({"fused_relayout": True} if args.fused else {})},
         "pct_bf16_peak": {"burst": value / peak_burst, "sustained": value / peak_sus,
                           "peaks": peak_kind},
         "roofline": {"kernel": (f"sp_attn_bwd over {args.ring} key chunks (statistics + tcgen05 "
@@ -452,7 +454,7 @@ def run_ours(args, w):
         "kernels": kernels,
         "ring": ring_info,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(w, args.ring) * args.steps,
+        "gpu_launches": launches_per_step(w, args.ring, args.fused) * args.steps,
         "clocks": clock_summary,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -475,6 +477,9 @@ def main(argv=None):
     ap.add_argument("--ring", type=int, default=0,
                     help="run the attention blockwise over this many key chunks (ring attention "
                          "on one GPU: chunked forward + merge, chunked backward)")
+    ap.add_argument("--fused", action="store_true",
+                    help="attention reads and writes the sequence shards directly (the "
+                         "regrouping done by the kernels' addressing, no relayout launches)")
     ap.add_argument("--key-mask", action="store_true",
                     help="give the workload's key padding as a general per-key mask "
                          "(the mask path of the kernels) instead of key lengths")

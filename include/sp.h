@@ -116,6 +116,12 @@ typedef struct sp_attn_params {
                                  entry bb takes part iff key_mask[bb*stride + j] != 0;
                                  16-byte aligned */
     int64_t key_mask_stride;  /* bytes between batch rows: a multiple of 16, >= sk */
+    int seq_shards;           /* 0 or 1: q, k, v, o, dout, dq, dk, dv use the strides above.
+                                 N >= 2: all eight are in the Ulysses sequence-shard layout
+                                 [N][B/N][sq/N][N*H][d] (contiguous; strides ignored), read
+                                 as B = N*b batch entries, entry g*b + bb being head group g
+                                 (heads g*H .. g*H+H-1) of batch row bb; needs sq == sk,
+                                 B % N == 0, sq % N == 0 and (sq/N) % 128 == 0 */
 } sp_attn_params;
 
 /*

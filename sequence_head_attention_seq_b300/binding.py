@@ -51,6 +51,7 @@ class SpAttnParams(ctypes.Structure):
         ("key_len", ctypes.c_void_p), ("softmax_scale", ctypes.c_float),
         ("dq_accumulate", ctypes.c_int),
         ("key_mask", ctypes.c_void_p), ("key_mask_stride", ctypes.c_int64),
+        ("seq_shards", ctypes.c_int),
     ]
 
 
@@ -211,20 +212,47 @@ def _mask_rows(key_mask, B: int, sk: int):
     return m
 
 
+def attn_dims(q):
+    """(B, sq, H, d, N) of a query tensor: [B][sq][H][d] (N = 1) or, in the sequence-shard
+    layout [N][b][s/N][N*H][d], B = N*b batch entries (entry g*b + bb = head group g of
+    batch row bb) over the full sequence sq = s."""
+    if q.dim() == 5:
+        N, b, sl, h, d = q.shape
+        if h % N:
+            raise ValueError("shard tensors need a head count divisible by N")
+        return N * b, N * sl, h // N, d, N
+    B, sq, H, d = q.shape
+    return B, sq, H, d, 1
+
+
 def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
                 softmax_scale=None, kv_offset: int = 0, key_mask=None) -> SpAttnParams:
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need_bf16_cuda(name, t)
-    B, sq, H, d = q.shape
-    if k.shape[0] != B or k.shape[2] != H or k.shape[3] != d or v.shape != k.shape:
-        raise ValueError("k and v must be [B][sk][H][d] matching q")
     p = SpAttnParams()
     p.q, p.k, p.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
-    p.q_stride = _strides(q, "q")
-    p.k_stride = _strides(k, "k")
-    p.v_stride = _strides(v, "v")
-    p.o_stride = _strides(o_like, "o")
-    p.B, p.H, p.sq, p.sk, p.d = B, H, sq, k.shape[1], d
+    B, sq, H, d, N = attn_dims(q)
+    if N > 1:
+        # sequence-shard layout: all tensors [N][b][s/N][N*H][d], contiguous
+        for name, t in (("k", k), ("v", v), ("o", o_like)):
+            if t.shape != q.shape:
+                raise ValueError(f"{name} must have the shard shape of q")
+        for name, t in (("q", q), ("k", k), ("v", v), ("o", o_like)):
+            if not t.is_contiguous():
+                raise ValueError(f"{name}: shard tensors must be contiguous")
+        zero = (ctypes.c_int64 * 3)(0, 0, 0)
+        p.q_stride = p.k_stride = p.v_stride = p.o_stride = zero
+        sk = sq
+    else:
+        if k.shape[0] != B or k.shape[2] != H or k.shape[3] != d or v.shape != k.shape:
+            raise ValueError("k and v must be [B][sk][H][d] matching q")
+        p.q_stride = _strides(q, "q")
+        p.k_stride = _strides(k, "k")
+        p.v_stride = _strides(v, "v")
+        p.o_stride = _strides(o_like, "o")
+        sk = k.shape[1]
+    p.seq_shards = N
+    p.B, p.H, p.sq, p.sk, p.d = B, H, sq, sk, d
     p.causal = 1 if causal else 0
     p.q_offset = int(q_offset)
     p.kv_offset = int(kv_offset)
@@ -236,7 +264,7 @@ def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
         p.key_len = None
     p.softmax_scale = float(softmax_scale) if softmax_scale is not None else 0.0
     if key_mask is not None:
-        m = _mask_rows(key_mask, B, k.shape[1])
+        m = _mask_rows(key_mask, B, sk)
         p.key_mask = m.data_ptr()
         p.key_mask_stride = m.stride(0)
         p._keep = m                     # keeps a padded copy alive while p is in use
@@ -248,9 +276,11 @@ def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
 
 def sp_attn_fwd(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,
                 softmax_scale=None, out=None, lse=None, kv_offset: int = 0, key_mask=None):
-    """out [B][sq][H][d] bf16 and lse [B][H][sq] fp32 (natural log)."""
+    """out (bf16, layout of q) and lse [B][H][sq] fp32 (natural log).  q, k, v are
+    [B][sq][H][d] / [B][sk][H][d], or all three [N][b][s/N][N*H][d] sequence shards (the
+    Ulysses regrouping is then done by the kernels' own addressing)."""
     lib = load()
-    B, sq, H, d = q.shape
+    B, sq, H, d, _ = attn_dims(q)
     if out is None:
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     if lse is None:

@@ -45,7 +45,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout,
-                                                       int64_t os0, int64_t os1, int64_t os2,
+                                                       const RowAddr ao,
                                                        const float* __restrict__ lse,
                                                        float* __restrict__ stats,
                                                        float* __restrict__ dq_acc, int B, int H,
@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   constexpr int kPer = D / 32;   // elements per lane
   float acc = 0.0f;
   if (i < sq) {
-    const int64_t off = b * os0 + i * os1 + h * os2 + lane * kPer;
+    const int64_t off = ao.off(b, static_cast<int>(i), h) + lane * kPer;
     if constexpr (kPer == 4) {
       const uint2 a = *reinterpret_cast<const uint2*>(o + off);
       const uint2 c = *reinterpret_cast<const uint2*>(dout + off);
@@ -107,8 +107,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dq_acc,
                                                              __nv_bfloat16* __restrict__ dq,
-                                                             int64_t qs0, int64_t qs1,
-                                                             int64_t qs2, int B, int H, int sq,
+                                                             const RowAddr aq, int B, int H, int sq,
                                                              int64_t rows, float scale) {
   // thread = 8 consecutive elements of one row
   constexpr int kVec = D / 8;
@@ -127,7 +126,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   out.y = pack_bf16x2(x.z * scale, x.w * scale);
   out.z = pack_bf16x2(y.x * scale, y.y * scale);
   out.w = pack_bf16x2(y.z * scale, y.w * scale);
-  *reinterpret_cast<uint4*>(dq + b * qs0 + i * qs1 + h * qs2 + c * 8) = out;
+  *reinterpret_cast<uint4*>(dq + aq.off(b, static_cast<int>(i), h) + c * 8) = out;
 }
 
 // ---------------------------------------------------------------- 2. main kernel
@@ -156,7 +155,7 @@ struct BwdKernelParams {
   float* dq_acc;          // [B][H][rows][D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int64_t k_stride[3], v_stride[3];
+  RowAddr aq, ak, av;     // row layouts of q and dO (TMA), k/dk, v/dv
   AttnGeom g;
   int64_t rows;
   int num_kv_tiles;
@@ -271,9 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tma_prefetch_desc(&p.tdo);
     tma_prefetch_desc(&p.tdq);
     mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
+    const TmaRow rk = tma_row(p.ak, b, kv0, h);
     for (int c = 0; c < kChunks; ++c) {
-      tma_load_4d(sm.k + c * 16384, &p.tk, &sm.kv_full, c * 64, h, kv0, b);
-      tma_load_4d(sm.v + c * 16384, &p.tv, &sm.kv_full, c * 64, h, kv0, b);
+      tma_load_5d(sm.k + c * 16384, &p.tk, &sm.kv_full, c * 64, rk.head, rk.row, rk.batch,
+                  rk.shard);
+      tma_load_5d(sm.v + c * 16384, &p.tv, &sm.kv_full, c * 64, rk.head, rk.row, rk.batch,
+                  rk.shard);
     }
     const float* st_base = p.stats + static_cast<int64_t>(bh) * 2 * p.rows;
     for (int it = 0; it < nq; ++it) {
@@ -281,14 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const int q0 = (m_start + it) * kRows;
       if (it >= 2 && !mbar_wait(&sm.q_empty[s], ((it >> 1) - 1) & 1, p.status, abort_flag)) break;
       // Q and the statistics first: the next S^T waits for them, dO is needed later
+      // (q and dout share their row geometry, so one set of coordinates serves both)
+      const TmaRow rq = tma_row(p.aq, b, q0, h);
       mbar_expect_tx(&sm.q_full[s], kTileBytes + 2 * kRows * 4);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_4d(sm.q[s] + c * 16384, &p.tq, &sm.q_full[s], c * 64, h, q0, b);
+        tma_load_5d(sm.q[s] + c * 16384, &p.tq, &sm.q_full[s], c * 64, rq.head, rq.row,
+                    rq.batch, rq.shard);
       bulk_load(sm.stats[s][0], st_base + q0, kRows * 4, &sm.q_full[s]);
       bulk_load(sm.stats[s][1], st_base + p.rows + q0, kRows * 4, &sm.q_full[s]);
       mbar_expect_tx(&sm.do_full[s], kTileBytes);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_4d(sm.dout[s] + c * 16384, &p.tdo, &sm.do_full[s], c * 64, h, q0, b);
+        tma_load_5d(sm.dout[s] + c * 16384, &p.tdo, &sm.do_full[s], c * 64, rq.head, rq.row,
+                    rq.batch, rq.shard);
     }
   } else if (warp == 1 && lane == 0 && nq > 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -528,10 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       if (ok) tc_fence_after();
     }
     const bool store = key < g.sk;
-    __nv_bfloat16* dk_row = p.dk + b * p.k_stride[0] + static_cast<int64_t>(key) * p.k_stride[1] +
-                            h * p.k_stride[2] + wg * (D / 2);
-    __nv_bfloat16* dv_row = p.dv + b * p.v_stride[0] + static_cast<int64_t>(key) * p.v_stride[1] +
-                            h * p.v_stride[2] + wg * (D / 2);
+    __nv_bfloat16* dk_row = p.dk + p.ak.off(b, key, h) + wg * (D / 2);
+    __nv_bfloat16* dv_row = p.dv + p.av.off(b, key, h) + wg * (D / 2);
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const uint32_t col = (which == 0 ? kColDK : kColDV) + wg * (D / 2);
@@ -586,13 +590,13 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
       if (g.d == 128)
         bwd_prep_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout),
-            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats,
+            a.ao, a.lse, a.row_stats,
             a.dq_accumulate ? nullptr : a.dq_acc, g.B, g.H,
             g.sq, rows);
       else
         bwd_prep_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout),
-            a.o_stride[0], a.o_stride[1], a.o_stride[2], a.lse, a.row_stats,
+            a.ao, a.lse, a.row_stats,
             a.dq_accumulate ? nullptr : a.dq_acc, g.B, g.H,
             g.sq, rows);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -610,10 +614,9 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     p.dq_acc = a.dq_acc;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
-    for (int i = 0; i < 3; ++i) {
-      p.k_stride[i] = a.k_stride[i];
-      p.v_stride[i] = a.v_stride[i];
-    }
+    p.aq = a.aq;
+    p.ak = a.ak;
+    p.av = a.av;
     p.g = g;
     p.rows = rows;
     p.num_kv_tiles = (g.sk + kKeys - 1) / kKeys;
@@ -646,12 +649,10 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     if (blocks > 0) {
       if (g.d == 128)
         bwd_dq_convert_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.q_stride[0], a.q_stride[1],
-            a.q_stride[2], g.B, g.H, g.sq, rows, g.scale);
+            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.aq, g.B, g.H, g.sq, rows, g.scale);
       else
         bwd_dq_convert_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.q_stride[0], a.q_stride[1],
-            a.q_stride[2], g.B, g.H, g.sq, rows, g.scale);
+            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.aq, g.B, g.H, g.sq, rows, g.scale);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }

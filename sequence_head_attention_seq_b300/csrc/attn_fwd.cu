@@ -54,7 +54,7 @@ struct FwdSmem {
 struct FwdKernelParams {
   CUtensorMap tq, tk, tv;
   __nv_bfloat16* o;
-  int64_t o_stride[3];
+  RowAddr aq, ak, ao;     // row layouts of q, k/v and o
   float* lse;
   AttnGeom g;
   int num_pairs;      // ceil(sq / 256)
@@ -169,19 +169,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int ntiles = ti[1].nblocks > 0 ? 2 : 1;
     mbar_expect_tx(&sm.q_full, kTileBytes * ntiles);
     for (int t = 0; t < ntiles; ++t)
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_4d(sm.q[t] + c * 16384, &p.tq, &sm.q_full, c * 64, h, ti[t].q0, b);
+      for (int c = 0; c < kChunks; ++c) {
+        const TmaRow r = tma_row(p.aq, b, ti[t].q0, h);
+        tma_load_5d(sm.q[t] + c * 16384, &p.tq, &sm.q_full, c * 64, r.head, r.row, r.batch,
+                    r.shard);
+      }
     // n counts the key blocks visited (stages and phases follow it)
     for (int j = next_vis(0), n = 0; j < nmax; j = next_vis(j + 1), ++n) {
       const int s = n % kStages;
       if (n >= kStages && !mbar_wait(&sm.kv_empty[s], ((n / kStages) - 1) & 1, p.status, abort_flag))
         break;
+      const TmaRow r = tma_row(p.ak, b, j * kKeys, h);
       mbar_expect_tx(&sm.k_full[s], kTileBytes);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_4d(sm.k[s] + c * 16384, &p.tk, &sm.k_full[s], c * 64, h, j * kKeys, b);
+        tma_load_5d(sm.k[s] + c * 16384, &p.tk, &sm.k_full[s], c * 64, r.head, r.row, r.batch,
+                    r.shard);
       mbar_expect_tx(&sm.v_full[s], kTileBytes);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_4d(sm.v[s] + c * 16384, &p.tv, &sm.v_full[s], c * 64, h, j * kKeys, b);
+        tma_load_5d(sm.v[s] + c * 16384, &p.tv, &sm.v_full[s], c * 64, r.head, r.row, r.batch,
+                    r.shard);
     }
   } else if (warp == 1 && lane == 0 && nmax > 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -381,8 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     // epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2
     if (qrow < g.sq) {
-      __nv_bfloat16* orow = p.o + b * p.o_stride[0] + static_cast<int64_t>(qrow) * p.o_stride[1] +
-                            h * p.o_stride[2];
+      __nv_bfloat16* orow = p.o + p.ao.off(b, qrow, h);
       float* lse_out = p.lse + (static_cast<int64_t>(b) * g.H + h) * g.sq + qrow;
       if (visited == 0 || !ok) {
         uint4 z = make_uint4(0, 0, 0, 0);
@@ -401,8 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_ld32(lane_base + o_col + c * 32, ov);
         tmem_ld_wait();
         if (qrow < g.sq && ok) {
-          __nv_bfloat16* orow = p.o + b * p.o_stride[0] +
-                                static_cast<int64_t>(qrow) * p.o_stride[1] + h * p.o_stride[2];
+          __nv_bfloat16* orow = p.o + p.ao.off(b, qrow, h);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -436,7 +440,9 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   p.tk = a.tk;
   p.tv = a.tv;
   p.o = static_cast<__nv_bfloat16*>(a.o);
-  for (int i = 0; i < 3; ++i) p.o_stride[i] = a.o_stride[i];
+  p.aq = a.aq;
+  p.ak = a.ak;
+  p.ao = a.ao;
   p.lse = a.lse;
   p.g = a.g;
   p.num_pairs = (a.g.sq + 2 * kRows - 1) / (2 * kRows);

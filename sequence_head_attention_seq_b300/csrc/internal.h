@@ -22,6 +22,7 @@ struct AttnGeom {
   const int32_t* key_len;     // device, may be null
   const uint8_t* key_mask;    // device [B][key_mask_stride] bytes, may be null
   int64_t key_mask_stride;
+  int seq_shards;             // 1: plain strided tensors; N > 1: sequence-shard layout
   float scale;                // softmax scale
   float scale_log2;           // scale * log2(e)
 };
@@ -29,10 +30,43 @@ struct AttnGeom {
 // Rows of the per-head statistics arrays in the backward workspace (sq rounded to 128).
 inline int64_t padded_rows(int sq) { return (static_cast<int64_t>(sq) + 127) / 128 * 128; }
 
-// 4-D TMA map over a [B][S][H][d] bf16 tensor (element strides for batch, seq,
-// head), box = 64 columns of d x 128 rows of S, 128-byte swizzle.
-bool encode_rows_map(CUtensorMap* map, const void* base, int d, int S, int H, int B,
-                     const int64_t stride[3]);
+// Where head j of sequence row t of attention batch entry e sits in a bf16 tensor with
+// head_dim contiguous (element offsets):
+//     off = (e / bi) * group + (e % bi) * batch + (t / sl) * shard + (t % sl) * row + j * head
+// The plain layout [B][S][H][d] with strides (s0, s1, s2) has bi = B, sl = S,
+// group = shard = 0.  The sequence-shard layout of the Ulysses step,
+// [N][b][s/N][N*H][d], read as N*b entries (entry g*b + bb = head group g of batch row
+// bb) has bi = b, sl = s/N, group = H*d (the group's first head), batch = (s/N)*N*H*d,
+// shard = b*(s/N)*N*H*d, row = N*H*d.  The tensor map of such a tensor is 5-D:
+// (d, heads, sl, bi, shards) with head coordinate (e / bi) * group_heads + j.
+struct RowAddr {
+  int64_t group, batch, shard, row, head;
+  int bi, sl;
+  int group_heads;          // group / head: the head coordinate of a group's first head
+  __host__ __device__ __forceinline__ int64_t off(int e, int t, int j) const {
+    return static_cast<int64_t>(e / bi) * group + static_cast<int64_t>(e % bi) * batch +
+           static_cast<int64_t>(t / sl) * shard + static_cast<int64_t>(t % sl) * row +
+           static_cast<int64_t>(j) * head;
+  }
+};
+
+// TMA coordinates (after the d chunk) of head j, row t of batch entry e.
+struct TmaRow {
+  int head, row, batch, shard;
+};
+__device__ __forceinline__ TmaRow tma_row(const RowAddr& a, int e, int t, int j) {
+  return TmaRow{(e / a.bi) * a.group_heads + j, t % a.sl, e % a.bi, t / a.sl};
+}
+
+// RowAddr of a plain [B][S][H][d] tensor with element strides (batch, seq, head).
+RowAddr plain_rows(const int64_t stride[3], int B, int S);
+// RowAddr of a sequence-shard tensor [N][b][S/N][N*H][d], contiguous.
+RowAddr shard_rows(int N, int b, int S, int H, int d);
+
+// 5-D TMA map over a bf16 tensor described by `a` (heads_total heads, `shards` sequence
+// shards), box = 64 columns of d x 128 rows of one shard, 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* map, const void* base, int d, int heads_total, int shards,
+                     const RowAddr& a);
 
 // 2-D TMA map over the fp32 dQ accumulator viewed as [rows_total][d], box = 32
 // columns x 32 rows, 128-byte swizzle (the backward reduces dQ tiles into it).
@@ -40,8 +74,9 @@ bool encode_acc_map(CUtensorMap* map, const float* base, int d, int64_t rows_tot
 
 struct FwdArgs {
   CUtensorMap tq, tk, tv;
+  RowAddr aq, ak;       // layouts of q (and o's row coordinates) and k/v
   void* o;
-  int64_t o_stride[3];
+  RowAddr ao;
   float* lse;
   AttnGeom g;
   uint32_t* status;
@@ -51,14 +86,13 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;
   CUtensorMap tdq;     // over dq_acc (encode_acc_map)
+  RowAddr aq, ak, av, ao;   // layouts of q/dq, k/dk, v/dv, o/dout
   const void* o;
   const void* dout;
-  int64_t o_stride[3];
   const float* lse;
   void* dq;
   void* dk;
   void* dv;
-  int64_t q_stride[3], k_stride[3], v_stride[3];
   float* dq_acc;      // workspace: [B][H][rows][d] fp32
   float* row_stats;   // workspace: [B][H][2][rows] fp32 (-lse*log2e, D)
   bool dq_accumulate; // keep dq_acc from the previous call instead of zeroing it

@@ -103,6 +103,14 @@ sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
     if (!aligned16(p->key_mask) || p->key_mask_stride % 16 != 0) return SP_ERR_MISALIGNED;
     if (p->key_mask_stride < p->sk) return SP_ERR_INVALID_ARG;
   }
+  if (p->seq_shards < 0) return SP_ERR_INVALID_ARG;
+  if (p->seq_shards > 1) {
+    // tensors in the sequence-shard layout: B = N * b entries, the full sequence on
+    // both sides, whole 128-row tiles per shard
+    const int N = p->seq_shards;
+    if (p->B % N != 0 || p->sq != p->sk || p->sq % N != 0) return SP_ERR_INVALID_ARG;
+    if ((p->sq / N) % 128 != 0) return SP_ERR_UNSUPPORTED;
+  }
   g->B = p->B;
   g->H = p->H;
   g->sq = p->sq;
@@ -115,6 +123,7 @@ sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
   g->key_len = p->key_len;
   g->key_mask = p->key_mask;
   g->key_mask_stride = p->key_mask != nullptr ? p->key_mask_stride : 0;
+  g->seq_shards = p->seq_shards > 1 ? p->seq_shards : 1;
   float scale = p->softmax_scale;
   if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(p->d));
   g->scale = scale;
@@ -141,19 +150,50 @@ WorkspaceLayout workspace_layout(const AttnGeom& g) {
 
 }  // namespace
 
-bool encode_rows_map(CUtensorMap* map, const void* base, int d, int S, int H, int B,
-                     const int64_t stride[3]) {
+RowAddr plain_rows(const int64_t stride[3], int B, int S) {
+  RowAddr a;
+  a.group = 0;
+  a.batch = stride[0];
+  a.shard = 0;
+  a.row = stride[1];
+  a.head = stride[2];
+  a.bi = B > 0 ? B : 1;
+  a.sl = S > 0 ? S : 1;
+  a.group_heads = 0;
+  return a;
+}
+
+RowAddr shard_rows(int N, int b, int S, int H, int d) {
+  const int64_t sl = S / N, heads = static_cast<int64_t>(N) * H;
+  RowAddr a;
+  a.head = d;
+  a.row = heads * d;
+  a.batch = sl * a.row;
+  a.shard = b * a.batch;
+  a.group = static_cast<int64_t>(H) * d;
+  a.bi = b;
+  a.sl = static_cast<int>(sl);
+  a.group_heads = H;
+  return a;
+}
+
+bool encode_rows_map(CUtensorMap* map, const void* base, int d, int heads_total, int shards,
+                     const RowAddr& a) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t legal = static_cast<cuuint64_t>(d) * 2;   // any 16-byte multiple works for size-1 dims
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H > 0 ? H : 1),
-                        static_cast<cuuint64_t>(S > 0 ? S : 1), static_cast<cuuint64_t>(B > 0 ? B : 1)};
-  cuuint64_t strides[3] = {H > 1 ? static_cast<cuuint64_t>(stride[2]) * 2 : legal,
-                           S > 1 ? static_cast<cuuint64_t>(stride[1]) * 2 : legal,
-                           B > 1 ? static_cast<cuuint64_t>(stride[0]) * 2 : legal};
-  cuuint32_t box[4] = {64, 1, 128, 1};
-  cuuint32_t elem[4] = {1, 1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+  // strides of size-1 dimensions are never used: any legal value (a 16-byte multiple)
+  const cuuint64_t legal = static_cast<cuuint64_t>(d) * 2;
+  const int heads = heads_total > 0 ? heads_total : 1;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(a.sl), static_cast<cuuint64_t>(a.bi),
+                        static_cast<cuuint64_t>(shards > 0 ? shards : 1)};
+  cuuint64_t strides[4] = {heads > 1 ? static_cast<cuuint64_t>(a.head) * 2 : legal,
+                           a.sl > 1 ? static_cast<cuuint64_t>(a.row) * 2 : legal,
+                           a.bi > 1 ? static_cast<cuuint64_t>(a.batch) * 2 : legal,
+                           shards > 1 ? static_cast<cuuint64_t>(a.shard) * 2 : legal};
+  cuuint32_t box[5] = {64, 1, 128, 1, 1};
+  cuuint32_t elem[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
                         strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -172,6 +212,31 @@ bool encode_acc_map(CUtensorMap* map, const float* base, int d, int64_t rows_tot
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Row layouts of the attention tensors: plain strided [B][S][H][d], or all eight in the
+// sequence-shard layout [N][B/N][S/N][N*H][d].
+struct Layouts {
+  RowAddr q, k, v, o;
+  int heads_total, shards;
+};
+
+Layouts layouts_of(const sp_attn_params* p, const AttnGeom& g) {
+  Layouts L;
+  if (g.seq_shards > 1) {
+    const int N = g.seq_shards;
+    L.q = L.k = L.v = L.o = shard_rows(N, g.B / N, g.sq, g.H, g.d);
+    L.heads_total = N * g.H;
+    L.shards = N;
+  } else {
+    L.q = plain_rows(p->q_stride, g.B, g.sq);
+    L.k = plain_rows(p->k_stride, g.B, g.sk);
+    L.v = plain_rows(p->v_stride, g.B, g.sk);
+    L.o = plain_rows(p->o_stride, g.B, g.sq);
+    L.heads_total = g.H;
+    L.shards = 1;
+  }
+  return L;
 }
 
 }  // namespace sp
@@ -198,12 +263,15 @@ sp_status sp_attn_fwd(const sp_attn_params* p, void* o, float* lse, void* stream
   if (!aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return SP_ERR_MISALIGNED;
   if (empty_problem(g)) return SP_OK;
   FwdArgs a;
-  if (!encode_rows_map(&a.tq, p->q, g.d, g.sq, g.H, g.B, p->q_stride) ||
-      !encode_rows_map(&a.tk, p->k, g.d, g.sk, g.H, g.B, p->k_stride) ||
-      !encode_rows_map(&a.tv, p->v, g.d, g.sk, g.H, g.B, p->v_stride))
+  const Layouts L = layouts_of(p, g);
+  if (!encode_rows_map(&a.tq, p->q, g.d, L.heads_total, L.shards, L.q) ||
+      !encode_rows_map(&a.tk, p->k, g.d, L.heads_total, L.shards, L.k) ||
+      !encode_rows_map(&a.tv, p->v, g.d, L.heads_total, L.shards, L.v))
     return SP_ERR_CUDA;
+  a.aq = L.q;
+  a.ak = L.k;
   a.o = o;
-  for (int i = 0; i < 3; ++i) a.o_stride[i] = p->o_stride[i];
+  a.ao = L.o;
   a.lse = lse;
   a.g = g;
   a.status = status_word();
@@ -236,21 +304,20 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
   if (workspace == nullptr || workspace_bytes < w.total) return SP_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SP_ERR_MISALIGNED;
   BwdArgs a;
+  const Layouts L = layouts_of(p, g);
   if (g.sq > 0 && g.sk > 0) {
-    if (!encode_rows_map(&a.tq, p->q, g.d, g.sq, g.H, g.B, p->q_stride) ||
-        !encode_rows_map(&a.tk, p->k, g.d, g.sk, g.H, g.B, p->k_stride) ||
-        !encode_rows_map(&a.tv, p->v, g.d, g.sk, g.H, g.B, p->v_stride) ||
-        !encode_rows_map(&a.tdo, dout, g.d, g.sq, g.H, g.B, p->o_stride))
+    if (!encode_rows_map(&a.tq, p->q, g.d, L.heads_total, L.shards, L.q) ||
+        !encode_rows_map(&a.tk, p->k, g.d, L.heads_total, L.shards, L.k) ||
+        !encode_rows_map(&a.tv, p->v, g.d, L.heads_total, L.shards, L.v) ||
+        !encode_rows_map(&a.tdo, dout, g.d, L.heads_total, L.shards, L.o))
       return SP_ERR_CUDA;
   }
+  a.aq = L.q;
+  a.ak = L.k;
+  a.av = L.v;
+  a.ao = L.o;
   a.o = o;
   a.dout = dout;
-  for (int i = 0; i < 3; ++i) {
-    a.o_stride[i] = p->o_stride[i];
-    a.q_stride[i] = p->q_stride[i];
-    a.k_stride[i] = p->k_stride[i];
-    a.v_stride[i] = p->v_stride[i];
-  }
   a.lse = lse;
   a.dq = dq;
   a.dk = dk;

@@ -22,39 +22,47 @@ class UlyssesAttention:
     def __init__(self, N: int, b: int, s: int, h: int, d: int, causal: bool = True,
                  key_len: torch.Tensor | None = None, softmax_scale: float | None = None,
                  device="cuda", timer=None, ring_chunks: int = 0,
-                 key_mask: torch.Tensor | None = None):
+                 key_mask: torch.Tensor | None = None, fused: bool = False):
         """`timer(name)`, if given, returns a context manager wrapped around each
         library call (used to bracket calls with CUDA events).  ring_chunks > 1 runs the
         attention blockwise over that many equal key chunks (ring attention) instead of
         in one call.  key_mask ([b][s] bool, True = key takes part) is a general key mask
-        per batch row, applied in every head group."""
+        per batch row, applied in every head group.  fused=True lets the attention kernels
+        read and write the sequence shards directly (the regrouping is done by their own
+        addressing) instead of running the two relayouts; N == 1 needs no regrouping."""
         if s % N or h % N:
             raise ValueError("s and h must be divisible by N")
+        if fused and ring_chunks > 1:
+            raise ValueError("ring attention runs on the head-group layout (fused=False)")
+        if ring_chunks > 1 and key_mask is not None:
+            raise ValueError("ring attention here takes key_len, not a general key mask")
         self.N, self.b, self.s, self.h, self.d = N, b, s, h, d
         self.causal = causal
         self.softmax_scale = softmax_scale
         self.timer = timer if timer is not None else (lambda name: contextlib.nullcontext())
+        self.direct = fused or N == 1          # attention straight on the shard tensors
         dev = torch.device(device)
         hl = h // N
-        gshape = (N, b, s, hl, d)
         bf = dict(dtype=torch.bfloat16, device=dev)
-        # key lengths per batch row, repeated for every head group (batch entry g*b + bb)
+        # key lengths / mask per batch row, repeated for every head group (entry g*b + bb)
         self.key_len = None if key_len is None else key_len.to(dev, torch.int32).repeat(N)
         self.key_mask = None if key_mask is None else key_mask.to(dev).repeat(N, 1)
-        self.qg, self.kg, self.vg = (torch.empty(gshape, **bf) for _ in range(3))
-        self.og = torch.empty(gshape, **bf)
-        self.dog = torch.empty(gshape, **bf)
-        self.dqg, self.dkg, self.dvg = (torch.empty(gshape, **bf) for _ in range(3))
         self.lse = torch.empty((N * b, hl, s), dtype=torch.float32, device=dev)
         sshape = (N, b, s // N, h, d)
         self.o = torch.empty(sshape, **bf)
         self.dq, self.dk, self.dv = (torch.empty(sshape, **bf) for _ in range(3))
-        ws = sp_attn_bwd_workspace_size(self._g(self.qg), self._g(self.kg), self._g(self.vg),
-                                        causal, 0, self.key_len, softmax_scale)
+        if not self.direct:
+            gshape = (N, b, s, hl, d)
+            self.qg, self.kg, self.vg = (torch.empty(gshape, **bf) for _ in range(3))
+            self.og = torch.empty(gshape, **bf)
+            self.dog = torch.empty(gshape, **bf)
+            self.dqg, self.dkg, self.dvg = (torch.empty(gshape, **bf) for _ in range(3))
+            like = self._g(self.qg)
+        else:
+            like = self._a(self.o)
+        ws = sp_attn_bwd_workspace_size(like, like, like, causal, 0, self.key_len, softmax_scale)
         self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         self.ring_chunks = int(ring_chunks)
-        if self.ring_chunks > 1 and key_mask is not None:
-            raise ValueError("ring attention here takes key_len, not a general key mask")
         if self.ring_chunks > 1:
             if s % self.ring_chunks:
                 raise ValueError("s must be divisible by ring_chunks")
@@ -66,59 +74,70 @@ class UlyssesAttention:
         """Group buffer [N][b][s][hl][d] viewed as attention batch [N*b][s][hl][d]."""
         return t.view(self.N * self.b, self.s, self.h // self.N, self.d)
 
+    def _a(self, t: torch.Tensor) -> torch.Tensor:
+        """A shard tensor as the attention kernels take it directly: [b][s][h][d] for one
+        shard, else the shard layout itself."""
+        return t.view(self.b, self.s, self.h, self.d) if self.N == 1 else t
+
     def _to_groups(self, shards, groups, name):
-        if self.N == 1:
-            for x, y in zip(shards, groups):
-                y.copy_(x)          # one shard is already the full sequence
-            return
         with self.timer(name):
             sp_relayout_seq2head(list(shards), self.N, outs=list(groups))
 
     def _to_shards(self, groups, shards, name):
-        if self.N == 1:
-            for x, y in zip(groups, shards):
-                y.copy_(x)
-            return
         with self.timer(name):
             sp_relayout_head2seq(list(groups), self.N, outs=list(shards))
 
+    def _attention_inputs(self):
+        if self.direct:
+            return self._a(self._q), self._a(self._k), self._a(self._v)
+        return self._g(self.qg), self._g(self.kg), self._g(self.vg)
+
     def forward(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> torch.Tensor:
         """q, k, v: [N][b][s/N][h][d] shards -> O shards (same layout)."""
-        self._to_groups((q, k, v), (self.qg, self.kg, self.vg), "seq2head_qkv")
+        self._q, self._k, self._v = q, k, v
+        if not self.direct:
+            self._to_groups((q, k, v), (self.qg, self.kg, self.vg), "seq2head_qkv")
+        aq, ak, av = self._attention_inputs()
         if self.ring_chunks > 1:
-            out, lse, _ = ring_attention_fwd(self._g(self.qg), self._g(self.kg), self._g(self.vg),
-                                             self.chunks, self.causal, 0, self.key_len,
-                                             self.softmax_scale, bufs=self.ring_bufs,
-                                             timer=self.timer)
-            self.og = out.view(self.og.shape)
+            out, lse, _ = ring_attention_fwd(aq, ak, av, self.chunks, self.causal, 0,
+                                             self.key_len, self.softmax_scale,
+                                             bufs=self.ring_bufs, timer=self.timer)
+            if self.direct:
+                self.o.copy_(out.view(self.o.shape))
+            else:
+                self.og = out.view(self.og.shape)
             self.lse = lse
         else:
+            out = self._a(self.o) if self.direct else self._g(self.og)
             with self.timer("attn_fwd"):
-                sp_attn_fwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self.causal,
-                            0, self.key_len, self.softmax_scale, out=self._g(self.og),
-                            lse=self.lse, key_mask=self.key_mask)
-        self._to_shards((self.og,), (self.o,), "head2seq_o")
+                sp_attn_fwd(aq, ak, av, self.causal, 0, self.key_len, self.softmax_scale,
+                            out=out, lse=self.lse, key_mask=self.key_mask)
+        if not self.direct:
+            self._to_shards((self.og,), (self.o,), "head2seq_o")
         return self.o
 
     def backward(self, dout: torch.Tensor):
-        """dout shards -> (dq, dk, dv) shards; uses the last forward's O and lse."""
-        self._to_groups((dout,), (self.dog,), "seq2head_do")
+        """dout shards -> (dq, dk, dv) shards; uses the last forward's inputs, O and lse."""
+        aq, ak, av = self._attention_inputs()
+        if self.direct:
+            ao, ado = self._a(self.o), self._a(dout)
+            grads = (self._a(self.dq), self._a(self.dk), self._a(self.dv))
+        else:
+            self._to_groups((dout,), (self.dog,), "seq2head_do")
+            ao, ado = self._g(self.og), self._g(self.dog)
+            grads = (self._g(self.dqg), self._g(self.dkg), self._g(self.dvg))
         if self.ring_chunks > 1:
-            ring_attention_bwd(self._g(self.qg), self._g(self.kg), self._g(self.vg),
-                               self._g(self.og), self.lse, self._g(self.dog), self.chunks,
-                               self.causal, 0, self.key_len, self.softmax_scale,
-                               dq=self._g(self.dqg), dk=self._g(self.dkg), dv=self._g(self.dvg),
-                               workspace=self.workspace, timer=self.timer)
+            ring_attention_bwd(aq, ak, av, ao, self.lse, ado, self.chunks, self.causal, 0,
+                               self.key_len, self.softmax_scale, dq=grads[0], dk=grads[1],
+                               dv=grads[2], workspace=self.workspace, timer=self.timer)
+        else:
+            with self.timer("attn_bwd"):
+                sp_attn_bwd(aq, ak, av, ao, self.lse, ado, self.causal, 0, self.key_len,
+                            self.softmax_scale, dq=grads[0], dk=grads[1], dv=grads[2],
+                            workspace=self.workspace, key_mask=self.key_mask)
+        if not self.direct:
             self._to_shards((self.dqg, self.dkg, self.dvg), (self.dq, self.dk, self.dv),
                             "head2seq_grads")
-            return self.dq, self.dk, self.dv
-        with self.timer("attn_bwd"):
-            sp_attn_bwd(self._g(self.qg), self._g(self.kg), self._g(self.vg), self._g(self.og),
-                        self.lse, self._g(self.dog), self.causal, 0, self.key_len,
-                        self.softmax_scale, dq=self._g(self.dqg), dk=self._g(self.dkg),
-                        dv=self._g(self.dvg), workspace=self.workspace, key_mask=self.key_mask)
-        self._to_shards((self.dqg, self.dkg, self.dvg), (self.dq, self.dk, self.dv),
-                        "head2seq_grads")
         return self.dq, self.dk, self.dv
 
 

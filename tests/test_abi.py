@@ -99,6 +99,10 @@ def _params(**kw):
     (dict(key_mask=FAKE_ODD, key_mask_stride=256), MISALIGNED),
     (dict(key_mask=FAKE, key_mask_stride=264), MISALIGNED),     # stride not a multiple of 16
     (dict(key_mask=FAKE, key_mask_stride=240), INVALID),        # stride < sk
+    (dict(seq_shards=-1), INVALID),
+    (dict(seq_shards=3), INVALID),                              # B = 1 not a multiple of 3
+    (dict(seq_shards=2, B=2, sk=512), INVALID),                 # shard layout needs sq == sk
+    (dict(seq_shards=4, B=4), UNSUPPORTED),                     # 256 / 4 = 64-row shards
     (dict(kv_offset=(1 << 30) - 100), UNSUPPORTED),   # kv_offset + sk above 2^30
     (dict(sq=-1), INVALID),
     (dict(B=-2), INVALID),

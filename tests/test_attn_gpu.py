@@ -209,16 +209,25 @@ def test_workload_full_heads(name):
         check_grad(_bits_to_f64(dqg[gi, bb, :, j])[None, :, None, :], rdq, tag + " dq")
         check_grad(_bits_to_f64(dkg[gi, bb, :, j])[None, :, None, :], rdk, tag + " dk")
         check_grad(_bits_to_f64(dvg[gi, bb, :, j])[None, :, None, :], rdv, tag + " dv")
-    _check_gradient_sums(step, w)
+    _check_gradient_sums(step, w, ins["dout"])
     if name == "tiny":
         _check_tiny_split_q(w, ins)
 
 
-def _check_gradient_sums(step, w):
+def _groups(step, w, name, shard_tensor):
+    """Head-group view [N*b][s][hl][d] of a step tensor: its group buffer when the step keeps
+    one, else (one shard, attention run on the shard itself) the shard tensor."""
+    if hasattr(step, name):
+        return getattr(step, name).float().view(w.N * w.b, w.s, w.h_local, w.d)
+    assert w.N == 1
+    return shard_tensor.float().view(w.b, w.s, w.h, w.d)
+
+
+def _check_gradient_sums(step, w, dout):
     """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per head, over every head (rows with keys)."""
-    dk = step.dkg.float().view(w.N * w.b, w.s, w.h_local, w.d)
-    dv = step.dvg.float().view(w.N * w.b, w.s, w.h_local, w.d)
-    do = step.dog.float().view(w.N * w.b, w.s, w.h_local, w.d)
+    dk = _groups(step, w, "dkg", step.dk)
+    dv = _groups(step, w, "dvg", step.dv)
+    do = _groups(step, w, "dog", dout)
     sk = dk.sum(1)
     norm_k = dk.square().sum(1).sqrt()
     assert (sk.abs() <= 0.05 * norm_k + 1e-3).all(), "sum_j dK_j must vanish"
@@ -290,4 +299,4 @@ def test_workload_sampled_rows(name, ring):
         _, rdk, rdv = orc.attn_bwd_rows(*tensors, 0, 0, 0, 0, keys[0], keys[1], True)
         check_grad(step.dkg[gi, 0, keys[0]:keys[1], j].double().cpu().numpy(), rdk, f"{tag} dk rows")
         check_grad(step.dvg[gi, 0, keys[0]:keys[1], j].double().cpu().numpy(), rdv, f"{tag} dv rows")
-    _check_gradient_sums(step, w)
+    _check_gradient_sums(step, w, ins["dout"])
