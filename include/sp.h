@@ -72,6 +72,26 @@ sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int nten
                                int N, int b, int s, int h, int d, void* stream);
 
 /*
+ * Packed Q/K/V (the long-context-attention issue names a packed-QKV variant of its
+ * attention, LongContextAttentionQKVPacked): one sequence-shard buffer holding all
+ * three, [N][b][s/N][3][h][d], regrouped into three head-group buffers in one launch.
+ *
+ *   qkv    : DEVICE bf16 [N][b][s/N][3][h][d]; Q, K, V at index 0, 1, 2 of each row
+ *   out[t] : DEVICE bf16 [N][b][s][h/N][d] for t = Q, K, V (HOST array of 3 pointers)
+ * Bit-exact copy, as sp_relayout_seq2head; errors as sp_relayout_seq2head (the three
+ * parts of qkv must be 16-byte aligned: h*d a multiple of 8).
+ */
+sp_status sp_relayout_seq2head_packed(const void* qkv, void* const* out, int N, int b, int s,
+                                      int h, int d, void* stream);
+
+/*
+ * Inverse: three head-group buffers (e.g. dQ, dK, dV) into one packed sequence-shard
+ * buffer [N][b][s/N][3][h][d].  in: HOST array of 3 DEVICE pointers.
+ */
+sp_status sp_relayout_head2seq_packed(const void* const* in, void* qkv, int N, int b, int s,
+                                      int h, int d, void* stream);
+
+/*
  * One attention problem.  Sources: "adv07: Sequence Parallel" (mini-vllm
  * tutorial), section 3 Q4: out[i] = softmax(q[i] K^T / sqrt(d)) V with a causal
  * mask that hides only future keys (j > i), a query shard masking by its GLOBAL

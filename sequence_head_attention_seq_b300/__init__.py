@@ -15,9 +15,11 @@ calls raise.
 """
 from .binding import (SpError, sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd,
                       sp_attn_merge, sp_get_device_status, sp_relayout_head2seq,
-                      sp_relayout_seq2head, sp_status_string)
+                      sp_relayout_head2seq_packed, sp_relayout_seq2head,
+                      sp_relayout_seq2head_packed, sp_status_string)
 from .pipeline import UlyssesAttention, ring_attention_bwd, ring_attention_fwd
 
 __all__ = ["SpError", "sp_attn_bwd", "sp_attn_bwd_workspace_size", "sp_attn_fwd", "sp_attn_merge",
            "sp_get_device_status", "sp_relayout_head2seq", "sp_relayout_seq2head",
+           "sp_relayout_seq2head_packed", "sp_relayout_head2seq_packed",
            "sp_status_string", "UlyssesAttention", "ring_attention_fwd", "ring_attention_bwd"]

@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED",
 MAX_RELAYOUT_TENSORS = 8
 
 # Every symbol include/sp.h declares.
-EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_attn_fwd",
+EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_relayout_seq2head_packed",
+           "sp_relayout_head2seq_packed", "sp_attn_fwd",
            "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_merge", "sp_attn_bwd_noalloc",
            "sp_get_device_status", "sp_status_string"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # SP_NOALLOC_SCRATCH_BYTES
@@ -92,6 +93,12 @@ def load(build_if_missing: bool = True):
             f = getattr(lib, name)
             f.argtypes = [vpp, vpp, i, i, i, i, i, i, ctypes.c_void_p]
             f.restype = i
+        lib.sp_relayout_seq2head_packed.argtypes = [ctypes.c_void_p, vpp, i, i, i, i, i,
+                                                    ctypes.c_void_p]
+        lib.sp_relayout_seq2head_packed.restype = i
+        lib.sp_relayout_head2seq_packed.argtypes = [vpp, ctypes.c_void_p, i, i, i, i, i,
+                                                    ctypes.c_void_p]
+        lib.sp_relayout_head2seq_packed.restype = i
         pp = ctypes.POINTER(SpAttnParams)
         lib.sp_attn_fwd.argtypes = [pp, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.sp_attn_fwd.restype = i
@@ -272,6 +279,53 @@ def make_params(q, k, v, o_like, causal: bool, q_offset: int = 0, key_len=None,
         p.key_mask = None
         p.key_mask_stride = 0
     return p
+
+
+def sp_relayout_seq2head_packed(qkv, N: int, outs=None):
+    """Packed sequence shards [N][b][s/N][3][h][d] -> Q, K, V head groups
+    [N][b][s][h/N][d] (one launch)."""
+    lib = load()
+    _need_bf16_cuda("qkv", qkv)
+    if qkv.dim() != 6 or qkv.shape[0] != N or qkv.shape[3] != 3 or not qkv.is_contiguous():
+        raise ValueError("qkv must be contiguous [N][b][s/N][3][h][d]")
+    _, b, sl, _, h, d = qkv.shape
+    s = N * sl
+    shape = (N, b, s, h // N, d)
+    if outs is None:
+        outs = [torch.empty(shape, dtype=torch.bfloat16, device=qkv.device) for _ in range(3)]
+    for n, t in enumerate(outs):
+        _need_bf16_cuda(f"out[{n}]", t)
+        if not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"outputs must be contiguous {shape}")
+    pout, keep = _ptr_array(outs)
+    rc = lib.sp_relayout_seq2head_packed(qkv.data_ptr(), pout, N, b, s, h, d,
+                                         _stream(qkv.device))
+    _check("sp_relayout_seq2head_packed", rc)
+    return outs
+
+
+def sp_relayout_head2seq_packed(groups, N: int, out=None):
+    """Three head-group tensors [N][b][s][h/N][d] -> packed shards [N][b][s/N][3][h][d]."""
+    lib = load()
+    if len(groups) != 3:
+        raise ValueError("three head-group tensors")
+    for n, t in enumerate(groups):
+        _need_bf16_cuda(f"in[{n}]", t)
+        if not t.is_contiguous() or t.shape != groups[0].shape or t.dim() != 5:
+            raise ValueError("inputs must be contiguous [N][b][s][h/N][d] of one shape")
+    _, b, s, hl, d = groups[0].shape
+    h = hl * N
+    shape = (N, b, s // N, 3, h, d)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.bfloat16, device=groups[0].device)
+    _need_bf16_cuda("out", out)
+    if not out.is_contiguous() or tuple(out.shape) != shape:
+        raise ValueError(f"out must be contiguous {shape}")
+    pin, keep = _ptr_array(list(groups))
+    rc = lib.sp_relayout_head2seq_packed(pin, out.data_ptr(), N, b, s, h, d,
+                                         _stream(out.device))
+    _check("sp_relayout_head2seq_packed", rc)
+    return out
 
 
 def sp_attn_fwd(q, k, v, causal: bool = True, q_offset: int = 0, key_len=None,

@@ -11,8 +11,11 @@ namespace sp {
 
 constexpr int kMaxRelayoutTensors = SP_MAX_RELAYOUT_TENSORS;
 
+// shard_row: element pitch of a shard-side row (0: h*d; 3*h*d for packed Q/K/V, whose
+// tensor t starts t*h*d elements into each row).
 cudaError_t launch_relayout(const void* const* in, void* const* out, int ntensors, int N, int b,
-                            int s, int h, int d, bool to_heads, cudaStream_t stream);
+                            int s, int h, int d, bool to_heads, cudaStream_t stream,
+                            int64_t shard_row = 0);
 
 // Problem geometry after validation (see sp_attn_params).
 struct AttnGeom {

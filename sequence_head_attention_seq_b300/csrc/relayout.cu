@@ -44,6 +44,8 @@ struct RelayoutArgs {
   uint8_t* out[kMaxRelayoutTensors];
   uint32_t N, b, s, sl, h, hl, d;
   uint32_t run_vecs;       // R / vector width
+  uint32_t shard_row_vecs; // shard-side row pitch in vectors: h*d, or 3*h*d for packed Q/K/V
+  uint64_t shard_row;      // the same pitch in elements
   uint32_t tile_rows;      // T
   uint32_t tiles_per_shard;
   FastDiv run_div;         // divide a vector index by run_vecs
@@ -55,7 +57,7 @@ __device__ __forceinline__ void copy_tile(const Vec* __restrict__ src_base, Vec*
   // Vector w of the tile: run = w / run_vecs, k = w % run_vecs.
   //   group side offset  : w                       (contiguous span)
   //   shard side offset  : run * (h*d/vec) + k     (runs at stride h*d)
-  const uint32_t shard_stride = a.run_vecs * a.N;   // (h*d)/vec = N runs per row
+  const uint32_t shard_stride = a.shard_row_vecs;   // shard-side row pitch
   for (uint32_t w0 = threadIdx.x; w0 < nvec; w0 += blockDim.x * kUnroll) {
     Vec v[kUnroll];
 #pragma unroll
@@ -101,8 +103,7 @@ __global__ void __launch_bounds__(256) relayout_kernel(RelayoutArgs a, int to_he
   const size_t R = static_cast<size_t>(a.hl) * a.d;
   // element offsets of the tile's first run on each side
   const size_t group_off = ((static_cast<size_t>(g) * a.b + bb) * a.s + t0) * R;
-  const size_t shard_off =
-      ((static_cast<size_t>(r) * a.b + bb) * a.sl + u0) * (static_cast<size_t>(a.h) * a.d) + g * R;
+  const size_t shard_off = ((static_cast<size_t>(r) * a.b + bb) * a.sl + u0) * a.shard_row + g * R;
   const uint32_t nvec = rows * a.run_vecs;
   const int t = blockIdx.y;
   if (to_heads) {
@@ -120,7 +121,8 @@ __global__ void __launch_bounds__(256) relayout_kernel(RelayoutArgs a, int to_he
 }  // namespace
 
 cudaError_t launch_relayout(const void* const* in, void* const* out, int ntensors, int N, int b,
-                            int s, int h, int d, bool to_heads, cudaStream_t stream) {
+                            int s, int h, int d, bool to_heads, cudaStream_t stream,
+                            int64_t shard_row) {
   RelayoutArgs a{};
   for (int t = 0; t < ntensors; ++t) {
     a.in[t] = static_cast<const uint8_t*>(in[t]);
@@ -134,9 +136,11 @@ cudaError_t launch_relayout(const void* const* in, void* const* out, int ntensor
   a.hl = h / N;
   a.d = d;
   const uint64_t R = static_cast<uint64_t>(a.hl) * d;
+  a.shard_row = shard_row > 0 ? static_cast<uint64_t>(shard_row) : static_cast<uint64_t>(h) * d;
   // widest vector that divides a run and keeps every run 16/8/4-byte aligned
   int vec_elems = (R % 8 == 0) ? 8 : (R % 4 == 0) ? 4 : (R % 2 == 0) ? 2 : 1;
   a.run_vecs = static_cast<uint32_t>(R / vec_elems);
+  a.shard_row_vecs = static_cast<uint32_t>(a.shard_row / vec_elems);
   // tile of about 32 KiB per (group, batch, shard) span
   uint64_t rows = (32768 / 2 + R - 1) / R;
   if (rows < 1) rows = 1;

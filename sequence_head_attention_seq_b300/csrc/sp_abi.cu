@@ -68,13 +68,21 @@ sp_status check_relayout(const void* const* in, void* const* out, int ntensors, 
 }
 
 sp_status relayout(const void* const* in, void* const* out, int ntensors, int N, int b, int s,
-                   int h, int d, bool to_heads, void* stream) {
+                   int h, int d, bool to_heads, void* stream, int64_t shard_row = 0) {
   const sp_status st = check_relayout(in, out, ntensors, N, b, s, h, d);
   if (st != SP_OK) return st;
   if (launch_relayout(in, out, ntensors, N, b, s, h, d, to_heads,
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                      static_cast<cudaStream_t>(stream), shard_row) != cudaSuccess)
     return SP_ERR_CUDA;
   return SP_OK;
+}
+
+// The three tensors of a packed [N][b][s/N][3][h][d] buffer: tensor t starts t*h*d
+// elements into every row of 3*h*d.
+void packed_parts(const void* qkv, int h, int d, const void* part[3]) {
+  const size_t step = static_cast<size_t>(h) * d * 2;
+  for (int t = 0; t < 3; ++t)
+    part[t] = qkv == nullptr ? nullptr : static_cast<const uint8_t*>(qkv) + t * step;
 }
 
 bool strides_ok(const int64_t st[3]) {
@@ -253,6 +261,24 @@ sp_status sp_relayout_seq2head(const void* const* in, void* const* out, int nten
 sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int ntensors, int N,
                                int b, int s, int h, int d, void* stream) {
   return relayout(in, out, ntensors, N, b, s, h, d, false, stream);
+}
+
+sp_status sp_relayout_seq2head_packed(const void* qkv, void* const* out, int N, int b, int s,
+                                      int h, int d, void* stream) {
+  if (h < 1 || d < 1) return SP_ERR_INVALID_ARG;
+  const void* in[3];
+  packed_parts(qkv, h, d, in);
+  return relayout(in, out, 3, N, b, s, h, d, true, stream, static_cast<int64_t>(3) * h * d);
+}
+
+sp_status sp_relayout_head2seq_packed(const void* const* in, void* qkv, int N, int b, int s,
+                                      int h, int d, void* stream) {
+  if (h < 1 || d < 1) return SP_ERR_INVALID_ARG;
+  const void* part[3];
+  packed_parts(qkv, h, d, part);
+  void* out[3] = {const_cast<void*>(part[0]), const_cast<void*>(part[1]),
+                  const_cast<void*>(part[2])};
+  return relayout(in, out, 3, N, b, s, h, d, false, stream, static_cast<int64_t>(3) * h * d);
 }
 
 sp_status sp_attn_fwd(const sp_attn_params* p, void* o, float* lse, void* stream) {

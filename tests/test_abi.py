@@ -184,3 +184,16 @@ def test_noalloc_refuses_dq_accumulation(lib):
     p = _params(dq_accumulate=1)
     assert lib.sp_attn_bwd_noalloc(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                    None) == INVALID
+
+
+def test_packed_relayout_validation(lib):
+    pout, keep = _arr(FAKE, FAKE * 2, FAKE * 3)
+    f = lib.sp_relayout_seq2head_packed
+    assert f(None, pout, 2, 1, 8, 4, 64, None) == INVALID           # no qkv buffer
+    assert f(FAKE, pout, 2, 1, 8, 3, 64, None) == INVALID           # h % N
+    assert f(FAKE_ODD, pout, 2, 1, 8, 4, 64, None) == MISALIGNED
+    assert f(FAKE, pout, 2, 1, 8, 4, 3, None) == MISALIGNED         # parts 24 bytes apart
+    pin, keep2 = _arr(FAKE, FAKE * 2, FAKE * 3)
+    g = lib.sp_relayout_head2seq_packed
+    assert g(pin, None, 2, 1, 8, 4, 64, None) == INVALID
+    assert g(pin, FAKE_ODD, 2, 1, 8, 4, 64, None) == MISALIGNED

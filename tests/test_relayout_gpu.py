@@ -81,3 +81,27 @@ def test_relayout_workloads(name):
                 got = g[gi, 0, t].view(torch.int16)
                 want = x[r, 0, u, gi * w.h_local:(gi + 1) * w.h_local].view(torch.int16)
                 assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("N,b,s,h,d", [
+    (2, 1, 128, 2, 64),
+    (4, 2, 64, 8, 128),
+    (3, 2, 12, 6, 8),
+    (2, 3, 10, 4, 2),         # 4-byte runs; each part starts 16 bytes into the row
+])
+def test_packed_relayout_matches_oracle(N, b, s, h, d):
+    """Packed [N][b][s/N][3][h][d] shards: each of the three parts regrouped exactly as the
+    oracle regroups it alone, and the packed inverse restores the buffer bit for bit."""
+    need_gpu()
+    orc = oracle.default()
+    qkv = _rand_bits((N, b, s // N, 3, h, d), 300 + s)
+    from sequence_head_attention_seq_b300 import (sp_relayout_head2seq_packed,
+                                                  sp_relayout_seq2head_packed)
+    groups = sp_relayout_seq2head_packed(qkv, N)
+    back = sp_relayout_head2seq_packed(groups, N)
+    torch.cuda.synchronize()
+    check_status()
+    for t in range(3):
+        part = qkv[:, :, :, t].contiguous()
+        assert np.array_equal(u16(groups[t]), orc.seq2head(u16(part), N, b, s, h, d)), t
+    assert np.array_equal(u16(back), u16(qkv))
