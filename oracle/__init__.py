@@ -233,6 +233,83 @@ class Oracle:
         return out
 
 
+# ---------------------------------------------------------------- projections and layer
+#
+# "Parallel multi-head attention", sections 2.1-2.3 and 3.1-3.2: the input is projected by
+# ColumnParallelLinear wq, wk, wv (nn.Linear, y = x W^T with W [out][in]), attention runs
+# per head, and the concatenated heads are projected by a RowParallelLinear wo.  On one
+# device the weights are whole; wq, wk, wv are stacked into one [3*h*d][dim] weight, so
+# the projection's output is the packed [..][3][h][d] layout.  Matrix products are
+# numpy's (a library primitive); the regrouping is the seq->head index formula written
+# with reshape/transpose.
+
+
+def linear_fwd(x, w):
+    """y = x W^T (fp64)."""
+    return _f64(x) @ _f64(w).T
+
+
+def linear_bwd(dy, x, w):
+    """(dx, dW) of y = x W^T: dx = dy W, dW = dy^T x (fp64, over all leading dims of x)."""
+    dy, x, w = _f64(dy), _f64(x), _f64(w)
+    dy2 = dy.reshape(-1, dy.shape[-1])
+    x2 = x.reshape(-1, x.shape[-1])
+    return (dy2 @ w).reshape(x.shape[:-1] + (w.shape[1],)), dy2.T @ x2
+
+
+def _groups_of(t, N):
+    """[N][b][s/N][h][d] shards -> [N][b][s][h/N][d] head groups (fp64)."""
+    n, b, sl, h, d = t.shape
+    full = t.transpose(1, 0, 2, 3, 4).reshape(b, n * sl, h, d)
+    return full.reshape(b, n * sl, N, h // N, d).transpose(2, 0, 1, 3, 4)
+
+
+def _shards_of(g, N):
+    """[N][b][s][h/N][d] head groups -> [N][b][s/N][h][d] shards (fp64)."""
+    n, b, s, hl, d = g.shape
+    full = g.transpose(1, 2, 0, 3, 4).reshape(b, s, n * hl, d)
+    return full.reshape(b, N, s // N, n * hl, d).transpose(1, 0, 2, 3, 4)
+
+
+class Layer:
+    """The attention layer of the sequence-parallel step on shards x [N][b][s/N][dim]:
+    qkv = x Wqkv^T, Ulysses regrouping, causal attention per head, regrouping back,
+    out = O Wo^T.  Weights: wqkv [3*h*d][dim], wo [dim][h*d]."""
+
+    def __init__(self, orc, N, h, d, causal=True):
+        self.orc, self.N, self.h, self.d, self.causal = orc, N, h, d, causal
+
+    def forward(self, x, wqkv, wo):
+        N, h, d = self.N, self.h, self.d
+        x = _f64(x)
+        n, b, sl, dim = x.shape
+        qkv = linear_fwd(x, wqkv).reshape(n, b, sl, 3, h, d)
+        groups = [_groups_of(qkv[:, :, :, t], N) for t in range(3)]     # [N][b][s][hl][d]
+        o_groups = np.empty_like(groups[0])
+        for g in range(N):
+            o_groups[g], _ = self.orc.attn_fwd(groups[0][g], groups[1][g], groups[2][g],
+                                               self.causal)
+        o = _shards_of(o_groups, N).reshape(n, b, sl, h * d)
+        self.saved = (x, wqkv, wo, groups, o)
+        return linear_fwd(o, wo)
+
+    def backward(self, dout):
+        """(dx, dwqkv, dwo) for the last forward."""
+        N, h, d = self.N, self.h, self.d
+        x, wqkv, wo, groups, o = self.saved
+        n, b, sl, _ = x.shape
+        do, dwo = linear_bwd(dout, o, wo)
+        do_groups = _groups_of(do.reshape(n, b, sl, h, d), N)
+        grads = [np.empty_like(groups[0]) for _ in range(3)]
+        for g in range(N):
+            dq, dk, dv = self.orc.attn_bwd(groups[0][g], groups[1][g], groups[2][g],
+                                           do_groups[g], self.causal)
+            grads[0][g], grads[1][g], grads[2][g] = dq, dk, dv
+        dqkv = np.stack([_shards_of(t, N) for t in grads], axis=3).reshape(n, b, sl, 3 * h * d)
+        dx, dwqkv = linear_bwd(dqkv, x, wqkv)
+        return dx, dwqkv, dwo
+
+
 def default() -> Oracle:
     """The oracle built from oracle.c in this directory."""
     return Oracle(_load())

@@ -494,11 +494,78 @@ def pin_merge_closed_forms(orc):
     assert not out.any() and np.all(l0 == -np.inf)
 
 
+def pin_linear_loops(orc):
+    """nn.Linear y = x W^T, dx = dy W, dW = dy^T x against explicit loops on tiny shapes
+    ("Parallel multi-head attention", sections 2.1 and 2.3: Column/RowParallelLinear)."""
+    import oracle as om
+    M, n_in, n_out = 5, 4, 3
+    x, w, dy = _rand((M, n_in), 210), _rand((n_out, n_in), 211), _rand((M, n_out), 212)
+    y = om.linear_fwd(x, w)
+    dx, dw = om.linear_bwd(dy, x, w)
+    for i in range(M):
+        for o in range(n_out):
+            assert abs(y[i, o] - sum(x[i, c] * w[o, c] for c in range(n_in))) <= 1e-13
+        for c in range(n_in):
+            assert abs(dx[i, c] - sum(dy[i, o] * w[o, c] for o in range(n_out))) <= 1e-13
+    for o in range(n_out):
+        for c in range(n_in):
+            assert abs(dw[o, c] - sum(dy[i, o] * x[i, c] for i in range(M))) <= 1e-13
+
+
+def pin_layer_identity_weights(orc):
+    """Identity projections (wq = wk = wv = wo = I): the layer is attention of the shards
+    with themselves as q, k and v, regrouped by the oracle's own seq->head formula."""
+    import oracle as om
+    N, b, s, h, d = 2, 1, 12, 4, 4
+    dim = h * d
+    x = _rand((N, b, s // N, dim), 220)
+    eye = np.eye(dim)
+    L = om.Layer(orc, N, h, d)
+    out = L.forward(x, np.concatenate([eye, eye, eye]), eye)
+    shards = x.reshape(N, b, s // N, h, d)
+    groups = om._groups_of(shards, N)
+    ref = np.empty_like(groups)
+    for g in range(N):
+        ref[g], _ = orc.attn_fwd(groups[g], groups[g], groups[g], True)
+    _close(out, om._shards_of(ref, N).reshape(x.shape), 1e-13, "identity-weight layer")
+    # the float regrouping agrees with the pinned 16-bit one
+    bits = np.arange(shards.size, dtype=np.uint16).reshape(shards.shape)
+    assert np.array_equal(om._groups_of(bits.astype(np.float64), N).astype(np.uint16),
+                          orc.seq2head(bits, N, b, s, h, d))
+
+
+def pin_layer_finite_differences(orc):
+    """Central differences of sum(dout * layer(x)) for dx, dWqkv and dWo."""
+    import oracle as om
+    N, b, s, h, d = 2, 1, 8, 2, 4
+    dim = 8
+    x = _rand((N, b, s // N, dim), 230)
+    wqkv, wo = _rand((3 * h * d, dim), 231, 0.5), _rand((dim, h * d), 232, 0.5)
+    dout = _rand((N, b, s // N, dim), 233)
+    L = om.Layer(orc, N, h, d)
+    L.forward(x, wqkv, wo)
+    dx, dwqkv, dwo = L.backward(dout)
+    eps = 1e-6
+    rng = np.random.default_rng(234)
+    for arr, grad, name in ((x, dx, "dx"), (wqkv, dwqkv, "dwqkv"), (wo, dwo, "dwo")):
+        for _ in range(6):
+            idx = tuple(rng.integers(0, n) for n in arr.shape)
+            old = arr[idx]
+            arr[idx] = old + eps
+            f1 = float(np.sum(dout * om.Layer(orc, N, h, d).forward(x, wqkv, wo)))
+            arr[idx] = old - eps
+            f0 = float(np.sum(dout * om.Layer(orc, N, h, d).forward(x, wqkv, wo)))
+            arr[idx] = old
+            num = (f1 - f0) / (2 * eps)
+            assert abs(num - grad[idx]) <= 1e-6 * max(1.0, abs(num)), (name, idx, num, grad[idx])
+
+
 ALL_PINS = [
     pin_sdpa_causal_square, pin_sdpa_masks, pin_finite_differences, pin_zero_q_uniform,
     pin_causal_row0, pin_constant_v, pin_one_and_two_keys, pin_softmax_rows,
     pin_key_padding_is_truncation, pin_gradient_sums, pin_empty_rows, pin_rows_api,
     pin_golden_causal_example, pin_golden_split_q, pin_negative_control,
     pin_relayout_golden, pin_relayout_torch, pin_merge_split_kv, pin_merge_closed_forms,
-    pin_sdpa_key_mask, pin_key_mask_special_cases,
+    pin_sdpa_key_mask, pin_key_mask_special_cases, pin_linear_loops,
+    pin_layer_identity_weights, pin_layer_finite_differences,
 ]
