@@ -234,6 +234,27 @@ typedef struct sp_merge_params {
 
 sp_status sp_attn_merge(const sp_merge_params* p, void* stream);
 
+/*
+ * The projections around attention, as nn.Linear products with W [out][in] (row-major,
+ * contiguous): "Parallel multi-head attention", sections 2.1-2.3 and 3.1, projects the
+ * input with ColumnParallelLinear wq, wk, wv and the attention output with a
+ * RowParallelLinear wo.  On one GPU the full weights are local; a single [3*h*d][dim]
+ * weight gives the packed [..][3][h][d] layout that sp_relayout_seq2head_packed takes.
+ *
+ *   sp_linear_fwd : y[M][out] = x[M][in] . W^T
+ *   sp_linear_bwd : dx[M][in] = dy[M][out] . W          (skipped when dx is NULL)
+ *                   dW[out][in] = dy^T . x, or += with accumulate_dw = 1 (skipped when
+ *                   dw is NULL)
+ * bf16 in and out, fp32 accumulation; plain GEMMs on cuBLASLt without workspace.
+ * All pointers DEVICE, 16-byte aligned.  Errors: M < 0, in or out < 1, accumulate_dw
+ * not 0/1, required pointers NULL -> SP_ERR_INVALID_ARG; in or out not a multiple of 8,
+ * misaligned pointers -> SP_ERR_MISALIGNED; a failed GEMM -> SP_ERR_CUDA.
+ */
+sp_status sp_linear_fwd(const void* x, const void* w, void* y, int M, int in, int out,
+                        void* stream);
+sp_status sp_linear_bwd(const void* dy, const void* x, const void* w, void* dx, void* dw, int M,
+                        int in, int out, int accumulate_dw, void* stream);
+
 /* Size of the device scratch array that sp_attn_bwd_noalloc uses (32 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -7,19 +7,23 @@ The computation lives in ``libsp.so`` (C ABI in ``include/sp.h``, CUDA kernels i
     sp_attn_fwd                                   attention forward (out + lse)
     sp_attn_bwd                                   attention backward (dq, dk, dv)
     sp_attn_merge                                 ring / blockwise: merge key-chunk results
+    sp_linear_fwd / sp_linear_bwd                 projections around attention (GEMMs)
     UlyssesAttention                              the whole step on shard tensors
     ring_attention_fwd / ring_attention_bwd       blockwise attention over key chunks
+    AttentionLayer                                projections + regrouping + attention
 
 Nothing here computes attention in Python; if the native library is missing the
 calls raise.
 """
 from .binding import (SpError, sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd,
-                      sp_attn_merge, sp_get_device_status, sp_relayout_head2seq,
+                      sp_attn_merge, sp_get_device_status, sp_linear_bwd, sp_linear_fwd,
+                      sp_relayout_head2seq,
                       sp_relayout_head2seq_packed, sp_relayout_seq2head,
                       sp_relayout_seq2head_packed, sp_status_string)
-from .pipeline import UlyssesAttention, ring_attention_bwd, ring_attention_fwd
+from .pipeline import AttentionLayer, UlyssesAttention, ring_attention_bwd, ring_attention_fwd
 
 __all__ = ["SpError", "sp_attn_bwd", "sp_attn_bwd_workspace_size", "sp_attn_fwd", "sp_attn_merge",
            "sp_get_device_status", "sp_relayout_head2seq", "sp_relayout_seq2head",
-           "sp_relayout_seq2head_packed", "sp_relayout_head2seq_packed",
-           "sp_status_string", "UlyssesAttention", "ring_attention_fwd", "ring_attention_bwd"]
+           "sp_relayout_seq2head_packed", "sp_relayout_head2seq_packed", "sp_linear_fwd",
+           "sp_linear_bwd",
+           "sp_status_string", "UlyssesAttention", "AttentionLayer", "ring_attention_fwd", "ring_attention_bwd"]

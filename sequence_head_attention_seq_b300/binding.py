@@ -29,7 +29,8 @@ MAX_RELAYOUT_TENSORS = 8
 # Every symbol include/sp.h declares.
 EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_relayout_seq2head_packed",
            "sp_relayout_head2seq_packed", "sp_attn_fwd",
-           "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_merge", "sp_attn_bwd_noalloc",
+           "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_merge", "sp_linear_fwd",
+           "sp_linear_bwd", "sp_attn_bwd_noalloc",
            "sp_get_device_status", "sp_status_string"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # SP_NOALLOC_SCRATCH_BYTES
 
@@ -110,6 +111,11 @@ def load(build_if_missing: bool = True):
         lib.sp_attn_bwd_noalloc.restype = i
         lib.sp_attn_merge.argtypes = [ctypes.POINTER(SpMergeParams), ctypes.c_void_p]
         lib.sp_attn_merge.restype = i
+        vp = ctypes.c_void_p
+        lib.sp_linear_fwd.argtypes = [vp, vp, vp, i, i, i, vp]
+        lib.sp_linear_fwd.restype = i
+        lib.sp_linear_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+        lib.sp_linear_bwd.restype = i
         lib.sp_get_device_status.argtypes = [ctypes.c_void_p]
         lib.sp_get_device_status.restype = i
         lib.sp_status_string.argtypes = [i]
@@ -459,6 +465,54 @@ def sp_attn_merge(o_part, lse_part, o_acc, lse_acc, init: bool, o_out=None):
     rc = lib.sp_attn_merge(ctypes.byref(p), _stream(o_part.device))
     _check("sp_attn_merge", rc)
     return o_acc, lse_acc
+
+
+def _rows(t: torch.Tensor, name: str, width: int):
+    """A contiguous bf16 CUDA tensor viewed as rows of `width` elements."""
+    _need_bf16_cuda(name, t)
+    if not t.is_contiguous() or t.shape[-1] != width:
+        raise ValueError(f"{name} must be contiguous with last dimension {width}")
+    return t.numel() // width
+
+
+def sp_linear_fwd(x, w, out=None):
+    """y = x W^T for W [out_features][in_features]; x [..., in] -> y [..., out]."""
+    lib = load()
+    n_out, n_in = w.shape
+    M = _rows(x, "x", n_in)
+    _rows(w, "w", n_in)
+    if out is None:
+        out = torch.empty((*x.shape[:-1], n_out), dtype=torch.bfloat16, device=x.device)
+    if _rows(out, "out", n_out) != M:
+        raise ValueError("out must hold one row per row of x")
+    rc = lib.sp_linear_fwd(x.data_ptr(), w.data_ptr(), out.data_ptr(), M, n_in, n_out,
+                           _stream(x.device))
+    _check("sp_linear_fwd", rc)
+    return out
+
+
+def sp_linear_bwd(dy, x, w, dx=None, dw=None, accumulate_dw: bool = False,
+                  need_dx: bool = True):
+    """dx = dy W and dW = dy^T x (or dW += dy^T x) for y = x W^T."""
+    lib = load()
+    n_out, n_in = w.shape
+    M = _rows(x, "x", n_in)
+    if _rows(dy, "dy", n_out) != M:
+        raise ValueError("dy must hold one row per row of x")
+    if need_dx and dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        if accumulate_dw:
+            raise ValueError("accumulate_dw needs the dw to add to")
+        dw = torch.empty_like(w)
+    if dx is not None and _rows(dx, "dx", n_in) != M:
+        raise ValueError("dx must have the shape of x")
+    _rows(dw, "dw", n_in)
+    rc = lib.sp_linear_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(),
+                           dx.data_ptr() if dx is not None else None, dw.data_ptr(), M, n_in,
+                           n_out, 1 if accumulate_dw else 0, _stream(x.device))
+    _check("sp_linear_bwd", rc)
+    return dx, dw
 
 
 def sp_get_device_status(device=None) -> int:

@@ -15,7 +15,9 @@ import contextlib
 import torch
 
 from .binding import (sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd, sp_attn_merge,
-                      sp_relayout_head2seq, sp_relayout_seq2head)
+                      sp_linear_bwd, sp_linear_fwd, sp_relayout_head2seq,
+                      sp_relayout_head2seq_packed, sp_relayout_seq2head,
+                      sp_relayout_seq2head_packed)
 
 
 class UlyssesAttention:
@@ -200,3 +202,81 @@ def ring_attention_bwd(q, k, v, out, lse, dout, chunks, causal=True, q_offset=0,
                         softmax_scale, dq=dq, dk=dk[:, lo:hi], dv=dv[:, lo:hi], workspace=ws,
                         kv_offset=lo, dq_accumulate=(n > 0))
     return dq, dk, dv
+
+
+class AttentionLayer:
+    """The attention layer of the sequence-parallel step ("Parallel multi-head attention",
+    sections 2-3: ColumnParallel q/k/v projections, attention per head, RowParallel
+    output projection) on sequence shards x [N][b][s/N][dim]:
+
+        qkv = x Wqkv^T          one GEMM into the packed [N][b][s/N][3][h][d] layout
+        Q, K, V groups          sp_relayout_seq2head_packed (one launch)
+        O groups                sp_attn_fwd
+        O shards                sp_relayout_head2seq
+        out = O Wo^T            one GEMM
+
+    and the backward back to dx, dWqkv, dWo.  wqkv [3*h*d][dim], wo [dim][h*d] (bf16)."""
+
+    def __init__(self, N: int, b: int, s: int, h: int, d: int, dim: int, causal: bool = True,
+                 device="cuda", timer=None):
+        if s % N or h % N:
+            raise ValueError("s and h must be divisible by N")
+        self.N, self.b, self.s, self.h, self.d, self.dim = N, b, s, h, d, dim
+        self.causal = causal
+        self.timer = timer if timer is not None else (lambda name: contextlib.nullcontext())
+        dev = torch.device(device)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        sl, hl = s // N, h // N
+        self.qkv = torch.empty((N, b, sl, 3, h, d), **bf)
+        self.groups = [torch.empty((N, b, s, hl, d), **bf) for _ in range(3)]
+        self.og = torch.empty((N, b, s, hl, d), **bf)
+        self.o = torch.empty((N, b, sl, h, d), **bf)
+        self.out = torch.empty((N, b, sl, dim), **bf)
+        self.lse = torch.empty((N * b, hl, s), dtype=torch.float32, device=dev)
+        self.do = torch.empty((N, b, sl, h, d), **bf)
+        self.dog = torch.empty((N, b, s, hl, d), **bf)
+        self.dgroups = [torch.empty((N, b, s, hl, d), **bf) for _ in range(3)]
+        self.dqkv = torch.empty((N, b, sl, 3, h, d), **bf)
+        self.dx = torch.empty((N, b, sl, dim), **bf)
+        self.dwqkv = torch.empty((3 * h * d, dim), **bf)
+        self.dwo = torch.empty((dim, h * d), **bf)
+        g = self._g(self.og)
+        ws = sp_attn_bwd_workspace_size(g, g, g, causal)
+        self.workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+
+    def _g(self, t):
+        return t.view(self.N * self.b, self.s, self.h // self.N, self.d)
+
+    def forward(self, x, wqkv, wo):
+        self._x, self._wqkv, self._wo = x, wqkv, wo
+        with self.timer("proj_qkv"):
+            sp_linear_fwd(x, wqkv, out=self.qkv.view(*x.shape[:-1], -1))
+        with self.timer("seq2head_qkv"):
+            sp_relayout_seq2head_packed(self.qkv, self.N, outs=self.groups)
+        with self.timer("attn_fwd"):
+            sp_attn_fwd(*(self._g(t) for t in self.groups), self.causal, out=self._g(self.og),
+                        lse=self.lse)
+        with self.timer("head2seq_o"):
+            sp_relayout_head2seq([self.og], self.N, outs=[self.o])
+        with self.timer("proj_o"):
+            sp_linear_fwd(self.o.view(*self.o.shape[:3], -1), wo, out=self.out)
+        return self.out
+
+    def backward(self, dout):
+        """-> (dx, dwqkv, dwo) for the last forward."""
+        o2 = self.o.view(*self.o.shape[:3], -1)
+        with self.timer("proj_o_bwd"):
+            sp_linear_bwd(dout, o2, self._wo, dx=self.do.view(o2.shape), dw=self.dwo)
+        with self.timer("seq2head_do"):
+            sp_relayout_seq2head([self.do], self.N, outs=[self.dog])
+        with self.timer("attn_bwd"):
+            sp_attn_bwd(*(self._g(t) for t in self.groups), self._g(self.og), self.lse,
+                        self._g(self.dog), self.causal, dq=self._g(self.dgroups[0]),
+                        dk=self._g(self.dgroups[1]), dv=self._g(self.dgroups[2]),
+                        workspace=self.workspace)
+        with self.timer("head2seq_grads"):
+            sp_relayout_head2seq_packed(self.dgroups, self.N, out=self.dqkv)
+        with self.timer("proj_qkv_bwd"):
+            sp_linear_bwd(self.dqkv.view(*self._x.shape[:-1], -1), self._x, self._wqkv,
+                          dx=self.dx, dw=self.dwqkv)
+        return self.dx, self.dwqkv, self.dwo

@@ -197,3 +197,16 @@ def test_packed_relayout_validation(lib):
     g = lib.sp_relayout_head2seq_packed
     assert g(pin, None, 2, 1, 8, 4, 64, None) == INVALID
     assert g(pin, FAKE_ODD, 2, 1, 8, 4, 64, None) == MISALIGNED
+
+
+def test_linear_validation(lib):
+    f, g = lib.sp_linear_fwd, lib.sp_linear_bwd
+    assert f(FAKE, FAKE, FAKE, -1, 64, 64, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, 4, 0, 64, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, 4, 60, 64, None) == MISALIGNED          # rows not 16-byte
+    assert f(None, FAKE, FAKE, 4, 64, 64, None) == INVALID
+    assert f(FAKE_ODD, FAKE, FAKE, 4, 64, 64, None) == MISALIGNED
+    assert f(FAKE, FAKE, FAKE, 0, 64, 64, None) == OK                  # no rows: nothing
+    assert g(FAKE, FAKE, FAKE, None, None, 4, 64, 64, 0, None) == INVALID   # nothing to do
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 2, None) == INVALID
+    assert g(FAKE, FAKE, FAKE, FAKE_ODD, FAKE, 4, 64, 64, 0, None) == MISALIGNED
