@@ -62,6 +62,13 @@ def step_flops(w) -> float:
     return 3.5 * attn_fwd_flops(w)          # forward + backward (2.5x forward)
 
 
+def proj_flops(w) -> float:
+    """Projections of the attention layer (hidden = h*d): forward 2*M*dim*3hd (q, k, v) +
+    2*M*hd*dim (output), backward twice that (input and weight gradients)."""
+    M, dim, hd = w.b * w.s, w.h * w.d, w.h * w.d
+    return 3 * (2.0 * M * dim * 3 * hd + 2.0 * M * hd * dim)
+
+
 def tensor_bytes(w) -> int:
     return w.b * w.s * w.h * w.d * 2
 
@@ -317,13 +324,29 @@ def run_ours(args, w):
         # the same right padding, expressed as a general per-key mask
         key_mask = torch.arange(w.s)[None, :] < key_len[:, None]
         key_len = None
-    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=key_len,
-                            device=device, timer=timer, ring_chunks=args.ring, key_mask=key_mask,
-                            fused=args.fused)
+    if args.layer:
+        # the whole attention layer with synthetic weights (hidden = h * d)
+        from sequence_head_attention_seq_b300 import AttentionLayer
+        dim = w.h * w.d
+        lshape = (w.N, w.b, w.s_local, dim)
+        x = workloads.randn_bf16(lshape, w.seed("q"), w.scale, device)
+        wqkv = workloads.randn_bf16((3 * w.h * w.d, dim), 1000 * w.index + 5, dim ** -0.5, device)
+        wo = workloads.randn_bf16((dim, w.h * w.d), 1000 * w.index + 6, (w.h * w.d) ** -0.5,
+                                  device)
+        ldout = workloads.randn_bf16(lshape, w.seed("dout"), 1.0, device)
+        step = AttentionLayer(w.N, w.b, w.s, w.h, w.d, dim, w.causal, device=device, timer=timer)
 
-    def one_step():
-        step.forward(ins["q"], ins["k"], ins["v"])
-        step.backward(ins["dout"])
+        def one_step():
+            step.forward(x, wqkv, wo)
+            step.backward(ldout)
+    else:
+        step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=key_len,
+                                device=device, timer=timer, ring_chunks=args.ring,
+                                key_mask=key_mask, fused=args.fused)
+
+        def one_step():
+            step.forward(ins["q"], ins["k"], ins["v"])
+            step.backward(ins["dout"])
 
     for _ in range(args.warmup):
         one_step()
@@ -352,11 +375,12 @@ def run_ours(args, w):
         raise RuntimeError(f"device status {status} after the timed region")
     total_ms = reduce_max(local_ms, device)
     ms_per_step = total_ms / args.steps
-    value = world * step_flops(w) * args.steps / (total_ms * 1e-3) / 1e12
+    flops = step_flops(w) + (proj_flops(w) if args.layer else 0.0)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
     # end to end through the public API: pinned host buffers in, results back out
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.layer:
         host_in = {n: ins[n].cpu().pin_memory() for n in ("q", "k", "v", "dout")}
         host_out = [torch.empty(step.o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(4)]
         dev_in = {n: torch.empty_like(ins[n]) for n in host_in}
@@ -419,6 +443,10 @@ def run_ours(args, w):
         elif n in ("attn_bwd", "ring_chunk_bwd"):
             entry["ms_per_step"] = per_step[n]
             entry["tflops"] = 2.5 * fwd_f / (per_step[n] * 1e-3) / 1e12
+        elif n.startswith("proj_"):
+            M, dim, hd = w.b * w.s, w.h * w.d, w.h * w.d
+            f = 2.0 * M * dim * (3 * hd if "qkv" in n else hd) * (2 if n.endswith("_bwd") else 1)
+            entry["tflops"] = f / (ms * 1e-3) / 1e12
         elif n == "ring_merge":
             entry["ms_per_step"] = per_step[n]
             nbytes = merge_bytes_per_step(w, args.ring)
@@ -440,7 +468,9 @@ def run_ours(args, w):
         "config": {**config_of(w, args.ring),
                    **({"key_mask": "right padding given as a general per-key mask"}
                       if args.key_mask else {}),
-                   **({"fused_relayout": True} if args.fused else {})},
+                   **({"fused_relayout": True} if args.fused else {}),
+                   **({"layer": "projections included (hidden = h*d); value = (attention + "
+                               "projection flops) / time"} if args.layer else {})},
         "pct_bf16_peak": {"burst": value / peak_burst, "sustained": value / peak_sus,
                           "peaks": peak_kind},
         "roofline": {"kernel": (f"sp_attn_bwd over {args.ring} key chunks (statistics + tcgen05 "
@@ -477,6 +507,9 @@ def main(argv=None):
     ap.add_argument("--ring", type=int, default=0,
                     help="run the attention blockwise over this many key chunks (ring attention "
                          "on one GPU: chunked forward + merge, chunked backward)")
+    ap.add_argument("--layer", action="store_true",
+                    help="the whole attention layer: q/k/v and output projections (hidden = "
+                         "h*d, synthetic weights) around the step; value counts their flops too")
     ap.add_argument("--fused", action="store_true",
                     help="attention reads and writes the sequence shards directly (the "
                          "regrouping done by the kernels' addressing, no relayout launches)")
