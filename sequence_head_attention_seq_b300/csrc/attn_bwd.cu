@@ -13,7 +13,8 @@
 //      chunks: its rows, o, lse and dout are the previous call's.  Bandwidth bound.
 //   2. bwd_main: one CTA per (batch entry, head, 128-key block), looping over the
 //      128-row query tiles that can see it (causal: from the diagonal down).  Two
-//      compute warpgroups each own 64 of a tile's query columns.
+//      compute warpgroups each own 64 of a tile's query columns.  P is kept in fp32
+//      registers between the P pass and the dS pass.
 //        S^T = K Q_i^T, dP^T = V dO_i^T        (A, B from shared memory, K-major;
 //                                               N = 128: an N = 64 product takes
 //                                               as long as an N = 128 one)
@@ -21,11 +22,11 @@
 //        dK += dS^T Q_i                        (dS^T K-major in smem, Q MN-major)
 //        dQ_i^T = K^T dS^T  (d = 128)          (K and the dS tile, both read MN-major)
 //        dQ_i   = dS K      (d = 64)
-//      dQ_i is read out of TMEM at once (so the next tile's dP^T can reuse the
-//      columns) and added into the fp32 workspace: for d = 128 straight from
-//      registers (TMEM lanes are head-dim indices, so a warp's 32 lanes add one
-//      contiguous 128-byte piece of a dQ row); for d = 64 staged in the warp's own
-//      slice of the dS tile and added by TMA tensor reduce-adds.
+//      dQ_i is read out of TMEM at once by a drain warpgroup (so the next tile's dP^T
+//      can reuse the columns) and added into the fp32 workspace: for d = 128 straight
+//      from registers (TMEM lanes are head-dim indices, so a warp's 32 lanes add one
+//      contiguous 128-byte piece of a dQ row); for d = 64 staged in the dS tile and
+//      added by TMA tensor reduce-adds.
 //   3. bwd_dq_convert: dq = bf16(scale * accumulator).  Bandwidth bound.
 #include <type_traits>
 
@@ -37,7 +38,15 @@ namespace {
 
 constexpr int kRows = 128;   // query rows per tile
 constexpr int kKeys = 128;   // keys per CTA
-constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 two compute warpgroups
+// warp 0 TMA, warp 1 MMA (warps 2, 3 idle), warps 4..11 two compute warpgroups, warps
+// 12..15 the dQ drain warpgroup
+constexpr int kThreads = 512;
+// Registers per thread after the split (launched with 65536 / 512 = 128 each).  Each
+// SM sub-partition holds one warp of every warpgroup: 72 + 152 + 152 + 136 = 512
+// registers per lane slot, its whole 16384-entry file; the 56 x 128 registers the first
+// warpgroup gives back are exactly the 24 x 256 + 8 x 128 the others take.
+constexpr uint32_t kRegsControl = 72, kRegsCompute = 152, kRegsDrain = 136;
+static_assert(kRegsControl + 2 * kRegsCompute + kRegsDrain == 4 * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- 1. row statistics
@@ -142,8 +151,8 @@ struct BwdSmem {
   alignas(1024) uint8_t ds[kKeys * kRows * 2];
   alignas(16) float stats[2][2][kRows];            // [stage][-lse*log2e | D][row]
   // q_full: Q tile + row statistics (needed first, by S^T); do_full: dO tile (dP^T, dV)
-  uint64_t kv_full, q_full[2], do_full[2], q_empty[2], s_full, pds[2], dq_full, dq_empty,
-      dkv_full, drain;
+  uint64_t kv_full, q_full[2], do_full[2], q_empty[2], s_full, dp_full, p_full[2], pds[2],
+      ds_empty, stage_free, dq_full, dq_empty, dkv_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -168,9 +177,13 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
   return n;
 }
 
-// Threads: warp 0 TMA, warp 1 MMA (+ TMEM), warps 2..5 and 6..9 = compute warpgroups
-// WG0 / WG1, each owning 64 of the 128 query columns of every tile (a warp reaches the
-// TMEM lanes 32 * (warp % 4) .. + 31, so any four consecutive warps cover all 128).
+// Threads: warp 0 TMA, warp 1 MMA (+ TMEM), warps 4..7 and 8..11 = compute warpgroups
+// WG0 / WG1, each owning 64 of the 128 query columns of every tile, warps 12..15 = the
+// dQ drain (a warp reaches the TMEM lanes 32 * (warp % 4) .. + 31, so any four
+// consecutive warps cover all 128).  The drain has its own warps because adding a dQ
+// tile into the L2-resident accumulator takes longer than computing P and dS for it
+// (the reductions run at the L2's reduction rate whatever the instruction width); with
+// their own warps they overlap the next tile's P and dS instead of delaying them.
 //
 // TMEM columns (128 lanes = the CTA's 128 keys):
 //   [0,128)   S^T (query half h in [64h, 64h+64)); each warpgroup writes its P^T (bf16)
@@ -179,19 +192,22 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
 //             indices, columns = queries) or dQ (d = 64: lanes = queries)
 //   [256,256+D) dK accumulator, [256+D,256+2D) dV accumulator
 // Per query tile i the MMA thread issues
-//   (dQ_{i-1} read out) dP^T_i | dV += P^T_0 dO_0, dK += dS^T_0 Q_0 | dQ_i |
-//   dV += P^T_1 dO_1, dK += dS^T_1 Q_1 | S^T_{i+1}
-// Writing dQ_i out of the SM is slow and competes with the tensor core for the
-// shared-memory data path; issuing dQ_i as soon as dS is complete lets its read-out
-// and reductions overlap the half-1 products, the next S^T and the next dP^T instead
-// of holding up the next dP^T.  The next S^T overwrites the P^T columns only after the
-// dV products that read them (tcgen05 MMAs of one thread run in issue order).
+//   (dQ_{i-1} read out) dP^T_i | (P^T_i half h in TMEM) dV += P^T_h dO_h, h = 0, 1 |
+//   S^T_{i+1} | (dS_i in shared memory) dQ_i, dK += dS^T Q_i
+// and each warpgroup, per tile, computes P from S^T (while dP^T runs), writes P^T and
+// signals it, then computes dS from dP^T (while dV and the next S^T run), then reads
+// dQ_i out of TMEM and adds it to the accumulator (while dK runs).  The tensor core thus
+// works on one product or another while the warpgroups compute, instead of waiting for
+// both halves of P and dS before any dV, dK or next-tile product can start.  The next
+// S^T overwrites the P^T columns only after the dV products that read them (tcgen05 MMAs
+// of one thread run in issue order), and the warpgroups write the next dS only after
+// the dK and dQ products of this tile have finished reading the dS tile.
 //
-// d = 64: dQ leaves through shared memory.  After the dQ product completes, the dS tile
-// has no reader left, so each compute warp stages its 32 query rows x 32 columns of dQ
-// in its own 4 KB slice of that tile (the slice it writes dS into) and one lane issues
-// a TMA reduce-add of the box into the accumulator.  The warp waits for TMA to finish
-// reading the slice before it writes the next tile's dS there.
+// d = 64: dQ leaves through shared memory.  After the dK and dQ products complete, the
+// dS tile has no reader left, so each drain warp stages its 32 query rows as two
+// 32 x 32 boxes in two 4 KB slices of that tile and one lane issues TMA reduce-adds of
+// them into the accumulator; once TMA has read them the drain signals stage_free, which
+// the compute warpgroups wait for before writing the next tile's dS.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ BwdKernelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -243,11 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.do_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.p_full[s], kKeys);
       mbar_init(&sm.pds[s], kKeys);
     }
     mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.ds_empty, 1);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_empty, 2 * kKeys);
+    mbar_init(&sm.stage_free, kKeys);
+    mbar_init(&sm.dq_empty, kKeys);
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
@@ -262,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
 
+  // Every CTA takes the same register split, whatever work it has; each warpgroup sets
+  // its limit at the top of its own branch.
+  if (warp < 4) {
+  setmaxnreg_dec<kRegsControl>();
   if (warp == 0 && lane == 0 && nq > 0) {
     // ------------------------------------------------------------ TMA producer
     tma_prefetch_desc(&p.tq);
@@ -317,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     if (ok) {
       tc_fence_after();
       issue_s(smem_u32(sm.q[0]));
+      mma_commit(&sm.s_full);
     }
     for (int it = 0; it < nq && ok; ++it) {
       const int s = it & 1;
@@ -331,50 +356,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mma_ss(tmem + kColDP, sdesc_sw128(v_addr + off, 16, 1024),
                sdesc_sw128(do_addr + off, 16, 1024), kIdS, kk > 0);
       }
-      mma_commit(&sm.s_full);
-      // dV += P^T dO and dK += dS^T Q for query half hf (K = 64 queries)
-      auto issue_dkv = [&](int hf) {
+      mma_commit(&sm.dp_full);
+      // dV += P^T dO over query half hf (K = 64 queries), as soon as that P^T is in TMEM
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!(ok = mbar_wait(&sm.p_full[hf], it & 1, p.status, abort_flag))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk) {
-          const uint32_t acc = (it > 0 || hf > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t qrow = hf * 8192 + kk * 2048;      // 16 query rows
+        for (int kk = 0; kk < kHalf / 16; ++kk)
           mma_ts(tmem + kColDV, tmem + hf * kHalf + kk * 8,
-                 sdesc_sw128(do_addr + qrow, 16384, 1024), kIdKV, acc);
-          mma_ss(tmem + kColDK, sdesc_sw128(ds_addr + hf * 16384 + kk * 32, 16, 1024),
-                 sdesc_sw128(q_addr + qrow, 16384, 1024), kIdKV, acc);
-        }
-      };
+                 sdesc_sw128(do_addr + hf * 8192 + kk * 2048, 16384, 1024), kIdKV,
+                 (it > 0 || hf > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (!ok) break;
+      // the next tile's S^T: its columns are free once the dV products above have read
+      // P^T (tcgen05 MMAs of one thread run in issue order); it runs while the
+      // warpgroups compute dS
+      if (it + 1 < nq) {
+        if (!(ok = mbar_wait(&sm.q_full[s ^ 1], ((it + 1) >> 1) & 1, p.status, abort_flag))) break;
+        tc_fence_after();
+        issue_s(smem_u32(sm.q[s ^ 1]));
+        mma_commit(&sm.s_full);
+      }
       if (!(ok = mbar_wait(&sm.pds[0], it & 1, p.status, abort_flag))) break;
-      tc_fence_after();
-      issue_dkv(0);
       if (!(ok = mbar_wait(&sm.pds[1], it & 1, p.status, abort_flag))) break;
       tc_fence_after();
+      // dK += dS^T Q over both query halves (K = 128 queries)
+      auto issue_dk = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          mma_ss(tmem + kColDK, sdesc_sw128(ds_addr + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                 sdesc_sw128(q_addr + kk * 2048, 16384, 1024), kIdKV, (it > 0 || kk > 0) ? 1u : 0u);
+      };
       // dQ, contracting over the 128 keys; K and the dS tile are both read MN-major
       if constexpr (D == 128) {
-        // dQ^T = K^T dS^T: A = K^T (head-dim contiguous), B = dS^T (queries contiguous)
+        // dQ^T = K^T dS^T: A = K^T (head-dim contiguous), B = dS^T (queries contiguous).
+        // Issued before dK so that its read-out and reductions overlap the dK products.
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           mma_ss(tmem + kColDQ, sdesc_sw128(k_addr + kk * 2048, 16384, 1024),
                  sdesc_sw128(ds_addr + kk * 2048, 16384, 1024), kIdQT, kk > 0);
         mma_commit(&sm.dq_full);
-        issue_dkv(1);
+        issue_dk();
       } else {
         // dQ = dS K: A = dS (queries contiguous), B = K (head-dim contiguous).  The
         // warpgroups stage dQ in the dS tile, so dq_full waits for dK's last read of it.
+        issue_dk();
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           mma_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
                  sdesc_sw128(k_addr + kk * 2048, 16384, 1024), kIdQ, kk > 0);
-        issue_dkv(1);
         mma_commit(&sm.dq_full);
       }
-      // Q_i and dO_i have no reader left: release the stage for tile i + 2's loads
+      // the dS tile and Q_i, dO_i have no reader left
+      mma_commit(&sm.ds_empty);
       mma_commit(&sm.q_empty[s]);
-      if (it + 1 < nq) {
-        if (!(ok = mbar_wait(&sm.q_full[s ^ 1], ((it + 1) >> 1) & 1, p.status, abort_flag))) break;
-        tc_fence_after();
-        issue_s(smem_u32(sm.q[s ^ 1]));
-      }
     }
     mma_commit(&sm.dkv_full);
     if (!ok) {
@@ -382,9 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       int never = 0;
       mbar_wait(&sm.drain, 0, p.status, &never);
     }
-  } else if (warp >= 2) {
-    // ------------------------------------------------------------ P / dS, dQ drain, epilogue
-    const int wg = (warp - 2) / 4;                   // query half owned by this warpgroup
+  }
+  } else if (warp < 12) {
+    setmaxnreg_inc<kRegsCompute>();
+    // ------------------------------------------------------------ P / dS, epilogue
+    const int wg = (warp - 4) / 4;                   // query half owned by this warpgroup
     const int quad = warp % 4;
     const int jj = quad * 32 + lane;                 // key row in tile == TMEM lane
     const int key = kv0 + jj;
@@ -404,11 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      if constexpr (D == 64) {
-        // this warp's slice of the dS tile held the previous tile's dQ box
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-      }
       const float* nlse2 = sm.stats[s][0] + wg * kHalf;   // -lse * log2(e)
       const float* Dv = sm.stats[s][1] + wg * kHalf;
       const int qh0 = q0 + wg * kHalf;               // first query row of this half
@@ -419,49 +451,82 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       const float4* nl4 = reinterpret_cast<const float4*>(nlse2);
       const float4* D4 = reinterpret_cast<const float4*>(Dv);
       const uint64_t scale2 = f2_pack(g.scale_log2, g.scale_log2);
-      // one copy of the loop per masking case, chosen once per tile (need_mask is uniform
-      // across the warpgroup): no branches inside, so independent column pairs interleave
-      auto p_ds_half = [&](auto masked) {
+      // P of this half's 64 columns, fp32 column pairs, kept for dS
+      uint64_t p2[kHalf / 2];
+      // one copy of each loop per masking case, chosen once per tile (need_mask is
+      // uniform across the warpgroup): no branches inside, so column pairs interleave
+      auto p_half = [&](auto masked) {
         constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          // 32 columns of S^T per round trip to TMEM
+          uint32_t sraw[32];
+          tmem_ld32(lane_base + s_col + ch * 32, sraw);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 l4 = nl4[ch * 8 + i4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int cc = i4 * 4 + h2 * 2;          // column pair within the chunk
+              // x = S * scale * log2(e) - lse * log2(e), two columns per instruction
+              const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sraw[cc]),
+                                                 __uint_as_float(sraw[cc + 1])),
+                                         scale2, h2 ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y));
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              float p0 = ex2(x0), p1 = ex2(x1);
+              if constexpr (kMasked) {
+                const int c = ch * 32 + cc;
+                p0 = (key_ok && c >= first_q) ? p0 : 0.0f;
+                p1 = (key_ok && c + 1 >= first_q) ? p1 : 0.0f;
+              }
+              p2[ch * 16 + i4 * 2 + h2] = f2_pack(p0, p1);
+              pk[i4 * 2 + h2] = pack_bf16x2(p0, p1);
+            }
+          }
+          tmem_st16(lane_base + s_col + ch * 16, pk);   // over S^T columns already read
+        }
+      };
+      if (need_mask)
+        p_half(std::true_type{});
+      else
+        p_half(std::false_type{});
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[wg]);
+      // dS = P (dP - D) once dP^T is in TMEM and the MMAs of the previous tile have
+      // finished reading the dS tile
+      ok = mbar_wait(&sm.dp_full, it & 1, p.status, abort_flag);
+      // (d = 64: and the drain has staged and sent the previous tile's dQ from it)
+      if (it > 0)
+        ok = ok && mbar_wait(D == 128 ? &sm.ds_empty : &sm.stage_free, (it - 1) & 1, p.status,
+                             abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        // 32 columns of S^T and dP^T per round trip to TMEM
-        uint32_t sraw[32], draw[32];
-        tmem_ld32(lane_base + s_col + ch * 32, sraw);
+        uint32_t draw[32];
         tmem_ld32(lane_base + dp_col + ch * 32, draw);
         tmem_ld_wait();
-        uint32_t pk[16], dk2[16];
+        uint32_t dk2[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 l4 = nl4[ch * 8 + i4];
           const float4 d4 = D4[ch * 8 + i4];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const int cc = i4 * 4 + h2 * 2;            // column pair within the chunk
-            // x = S * scale * log2(e) - lse * log2(e), two columns per instruction
-            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sraw[cc]),
-                                               __uint_as_float(sraw[cc + 1])),
-                                       scale2, h2 ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y));
-            float x0, x1;
-            f2_unpack(x2, x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
-            if constexpr (kMasked) {
-              const int c = ch * 32 + cc;
-              p0 = (key_ok && c >= first_q) ? p0 : 0.0f;
-              p1 = (key_ok && c + 1 >= first_q) ? p1 : 0.0f;
-            }
-            const uint64_t p2 = f2_pack(p0, p1);
-            // dS = P (dP - D)
+            const int cc = i4 * 4 + h2 * 2;
             const uint64_t ds2 = f2_mul(
-                p2, f2_sub(f2_pack(__uint_as_float(draw[cc]), __uint_as_float(draw[cc + 1])),
-                           h2 ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y)));
+                p2[ch * 16 + i4 * 2 + h2],
+                f2_sub(f2_pack(__uint_as_float(draw[cc]), __uint_as_float(draw[cc + 1])),
+                       h2 ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y)));
             float d0, d1;
             f2_unpack(ds2, d0, d1);
-            pk[i4 * 2 + h2] = pack_bf16x2(p0, p1);
             dk2[i4 * 2 + h2] = pack_bf16x2(d0, d1);
           }
         }
-        tmem_st16(lane_base + s_col + ch * 16, pk);    // over S^T columns already read
         // dS row into the swizzled [key][query] chunk of this half: 4 x 16-byte units
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -469,62 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
           *dst = make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
         }
       }
-      };
-      if (need_mask)
-        p_ds_half(std::true_type{});
-      else
-        p_ds_half(std::false_type{});
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.pds[wg]);
-      ok = mbar_wait(&sm.dq_full, it & 1, p.status, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      if constexpr (D == 128) {
-        // dQ^T is ready: lane jj holds head-dim index jj; this warpgroup takes its 64 query
-        // columns out of TMEM, releases them, then adds them row by row (a warp's lanes
-        // cover 32 consecutive head-dim entries of one query row: one 128-byte piece)
-        uint32_t r[2][32];
-        tmem_ld32(lane_base + kColDQ + wg * kHalf, r[0]);
-        tmem_ld32(lane_base + kColDQ + wg * kHalf + 32, r[1]);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&sm.dq_empty);
-        float* dst = p.dq_acc + (static_cast<int64_t>(bh) * p.rows + q0 + wg * kHalf) * D + jj;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) red_add(dst + (h2 * 32 + i) * D, __uint_as_float(r[h2][i]));
-      } else {
-        // dQ is ready: lane jj holds query row q0 + jj; this warpgroup takes its 32 of the
-        // 64 head-dim columns out of TMEM and releases them
-        uint32_t r[32];
-        tmem_ld32(lane_base + kColDQ + wg * 32, r);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&sm.dq_empty);
-        // stage the warp's 32 rows x 32 columns (128-byte swizzle) in its slice of the
-        // dS tile, which the completed dQ product no longer reads, and reduce it with TMA
-        uint8_t* stage = sm.ds + wg * 16384 + quad * 4096;
-        uint8_t* srow = stage + lane * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) * 16)) =
-              make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_2d(&p.tdq, stage, wg * 32,
-                            static_cast<int>(static_cast<int64_t>(bh) * p.rows) + q0 + quad * 32);
-          bulk_commit();
-        }
-      }
     }
-    // the accumulator adds must be complete (and the slice read) before the CTA exits
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
     // epilogue: dK = scale * acc, dV = acc (zero when no query row sees this key block);
     // each warpgroup writes its half of the d columns
     const bool have = nq > 0;
@@ -563,6 +576,70 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         }
       }
     }
+  } else {
+    setmaxnreg_inc<kRegsDrain>();
+    // ------------------------------------------------------------ dQ drain
+    const int quad = warp % 4;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    bool ok = true;
+    for (int it = 0; it < nq; ++it) {
+      const int q0 = (m_start + it) * kRows;
+      ok = mbar_wait(&sm.dq_full, it & 1, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if constexpr (D == 128) {
+        // dQ^T: lane = head-dim index quad * 32 + lane, columns = the tile's 128 queries.
+        // All of it leaves TMEM before the release (the next dP^T waits for it); then it
+        // is added row by row: a warp's lanes cover 32 consecutive head-dim entries of one
+        // query row, one 128-byte piece
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kColDQ + c * 32, r[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        float* dst = p.dq_acc + (static_cast<int64_t>(bh) * p.rows + q0) * D + quad * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) red_add(dst + (c * 32 + i) * D, __uint_as_float(r[c][i]));
+      } else {
+        // dQ: lane = query row q0 + quad * 32 + lane, columns = the 64 head-dim entries
+        uint32_t r[2][32];
+        tmem_ld32(lane_base + kColDQ, r[0]);
+        tmem_ld32(lane_base + kColDQ + 32, r[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        // stage the warp's 32 rows as two 32 x 32 boxes (128-byte swizzle) in its two
+        // slices of the dS tile, which the completed dK and dQ products no longer read,
+        // reduce them into the accumulator with TMA, and hand the tile back once TMA has
+        // read them
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint8_t* srow = sm.ds + c * 16384 + quad * 4096 + lane * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) * 16)) =
+                make_uint4(r[c][4 * u], r[c][4 * u + 1], r[c][4 * u + 2], r[c][4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row = static_cast<int>(static_cast<int64_t>(bh) * p.rows) + q0 + quad * 32;
+          tma_reduce_add_2d(&p.tdq, sm.ds + quad * 4096, 0, row);
+          tma_reduce_add_2d(&p.tdq, sm.ds + 16384 + quad * 4096, 32, row);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        __syncwarp();
+        mbar_arrive(&sm.stage_free);
+      }
+    }
+    // the accumulator adds must be complete before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -660,3 +737,4 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace sp
+
