@@ -283,6 +283,66 @@ sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o, const floa
                               const void* dout, void* dq, void* dk, void* dv, void* stream);
 
 /*
+ * One Ulysses attention step (forward and backward) on HOST-resident shards, with the
+ * host<->device transfers overlapped with the attention kernels.  "Parallel multi-head
+ * attention", section 2.2, and the long-context-attention issue "关于数据分割和合并":
+ * each head group needs its heads from every sequence shard.  Here the copy engines
+ * perform that regrouping: head group g of a tensor is moved by 2-D copies (N*b runs of
+ * s/N rows of (h/N)*d elements at a pitch of h*d; one copy when b = 1) between the host
+ * shard layout and a head-major device buffer, and back for the results.  Group g's
+ * copies in, its forward and backward on `stream`, and its copies out run on three
+ * streams with group g+1's transfers overlapping group g's kernels (two buffer slots).
+ *
+ * The results equal those of sp_relayout_seq2head, sp_attn_fwd, sp_relayout_head2seq,
+ * sp_relayout_seq2head (dout), sp_attn_bwd and sp_relayout_head2seq on the same data:
+ * every head group is the independent attention problem [b][s][h/N][d].
+ *
+ * q, k, v, dout   : HOST bf16 [N][b][s/N][h][d] (shard r = sequence rows r*s/N ..),
+ *                   PAGE-LOCKED (cudaHostAlloc / cudaHostRegister), read only.
+ * o, dq, dk, dv   : HOST bf16, same layout, page-locked; written.  Valid once `stream`
+ *                   has reached the point this call enqueued up to.
+ * key_len         : NULL or DEVICE int32 [b] (keys of batch row bb: j < key_len[bb]).
+ * softmax_scale   : <= 0 selects 1/sqrt(d).
+ * workspace       : DEVICE, >= sp_ulysses_host_workspace_size(...) bytes, 256-byte
+ *                   aligned, owned by the caller (two slots of eight group tensors, the
+ *                   lse, and the backward workspace).
+ * stream          : the kernels run on it, and it waits for the last result to reach
+ *                   the host.  h2d_stream, d2h_stream: two further streams, distinct from
+ *                   each other and from `stream`, non-blocking (cudaStreamNonBlocking)
+ *                   for the transfers to overlap; both first wait for the work already
+ *                   queued on `stream`.
+ * The call creates a few CUDA events and releases them before it returns (their
+ * pending records complete on their own); it allocates no memory and does not
+ * synchronise the host.
+ * Errors: N, b, s, h < 1, s % N or h % N != 0, causal not 0/1, a NULL pointer or
+ *         stream, repeated streams, a host pointer that is not page-locked host memory
+ *         -> SP_ERR_INVALID_ARG; d not 64/128 -> SP_ERR_UNSUPPORTED; workspace too
+ *         small -> SP_ERR_WORKSPACE, misaligned -> SP_ERR_MISALIGNED; a failed CUDA
+ *         call -> SP_ERR_CUDA (work already queued by this call then still runs).
+ */
+typedef struct sp_ulysses_host_params {
+    int N, b, s, h, d;        /* shards, batch rows, full sequence, heads, head_dim */
+    int causal;               /* 0 or 1 */
+    float softmax_scale;
+    const int32_t* key_len;   /* NULL or DEVICE [b] */
+    const void* q;            /* HOST, page-locked: inputs */
+    const void* k;
+    const void* v;
+    const void* dout;
+    void* o;                  /* HOST, page-locked: results */
+    void* dq;
+    void* dk;
+    void* dv;
+} sp_ulysses_host_params;
+
+/* Device workspace bytes of sp_ulysses_step_host; 0 on invalid arguments. */
+size_t sp_ulysses_host_workspace_size(int N, int b, int s, int h, int d, int causal);
+
+sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
+                               size_t workspace_bytes, void* stream, void* h2d_stream,
+                               void* d2h_stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that the
  * kernels set when a bounded device-side wait gives up (SP_ERR_TIMEOUT) or a
  * launch-time invariant fails inside a kernel.  SP_ERR_CUDA if the stream

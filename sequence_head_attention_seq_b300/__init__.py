@@ -9,6 +9,7 @@ The computation lives in ``libsp.so`` (C ABI in ``include/sp.h``, CUDA kernels i
     sp_attn_merge                                 ring / blockwise: merge key-chunk results
     sp_linear_fwd / sp_linear_bwd                 projections around attention (GEMMs)
     UlyssesAttention                              the whole step on shard tensors
+    UlyssesHostStep / sp_ulysses_step_host        the step on host shards, transfers overlapped
     ring_attention_fwd / ring_attention_bwd       blockwise attention over key chunks
     AttentionLayer                                projections + regrouping + attention
 
@@ -19,11 +20,15 @@ from .binding import (SpError, sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_
                       sp_attn_merge, sp_get_device_status, sp_linear_bwd, sp_linear_fwd,
                       sp_relayout_head2seq,
                       sp_relayout_head2seq_packed, sp_relayout_seq2head,
-                      sp_relayout_seq2head_packed, sp_status_string)
-from .pipeline import AttentionLayer, UlyssesAttention, ring_attention_bwd, ring_attention_fwd
+                      sp_relayout_seq2head_packed, sp_status_string,
+                      sp_ulysses_host_workspace_size, sp_ulysses_step_host)
+from .pipeline import (AttentionLayer, UlyssesAttention, UlyssesHostStep, ring_attention_bwd,
+                       ring_attention_fwd)
 
 __all__ = ["SpError", "sp_attn_bwd", "sp_attn_bwd_workspace_size", "sp_attn_fwd", "sp_attn_merge",
            "sp_get_device_status", "sp_relayout_head2seq", "sp_relayout_seq2head",
            "sp_relayout_seq2head_packed", "sp_relayout_head2seq_packed", "sp_linear_fwd",
            "sp_linear_bwd",
-           "sp_status_string", "UlyssesAttention", "AttentionLayer", "ring_attention_fwd", "ring_attention_bwd"]
+           "sp_status_string", "sp_ulysses_host_workspace_size", "sp_ulysses_step_host",
+           "UlyssesAttention", "UlyssesHostStep", "AttentionLayer", "ring_attention_fwd",
+           "ring_attention_bwd"]

@@ -30,7 +30,8 @@ MAX_RELAYOUT_TENSORS = 8
 EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_relayout_seq2head_packed",
            "sp_relayout_head2seq_packed", "sp_attn_fwd",
            "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_merge", "sp_linear_fwd",
-           "sp_linear_bwd", "sp_attn_bwd_noalloc",
+           "sp_linear_bwd", "sp_attn_bwd_noalloc", "sp_ulysses_host_workspace_size",
+           "sp_ulysses_step_host",
            "sp_get_device_status", "sp_status_string"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # SP_NOALLOC_SCRATCH_BYTES
 
@@ -65,6 +66,19 @@ class SpMergeParams(ctypes.Structure):
         ("o_part", ctypes.c_void_p), ("part_stride", ctypes.c_int64 * 3),
         ("lse_part", ctypes.c_void_p), ("o_acc", ctypes.c_void_p), ("lse_acc", ctypes.c_void_p),
         ("o_out", ctypes.c_void_p), ("out_stride", ctypes.c_int64 * 3),
+    ]
+
+
+class SpUlyssesHostParams(ctypes.Structure):
+    """Mirror of sp_ulysses_host_params."""
+    _fields_ = [
+        ("N", ctypes.c_int), ("b", ctypes.c_int), ("s", ctypes.c_int), ("h", ctypes.c_int),
+        ("d", ctypes.c_int), ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+        ("key_len", ctypes.c_void_p),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("dout", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+        ("dv", ctypes.c_void_p),
     ]
 
 
@@ -116,6 +130,11 @@ def load(build_if_missing: bool = True):
         lib.sp_linear_fwd.restype = i
         lib.sp_linear_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
         lib.sp_linear_bwd.restype = i
+        lib.sp_ulysses_host_workspace_size.argtypes = [i, i, i, i, i, i]
+        lib.sp_ulysses_host_workspace_size.restype = ctypes.c_size_t
+        lib.sp_ulysses_step_host.argtypes = [ctypes.POINTER(SpUlyssesHostParams), vp,
+                                             ctypes.c_size_t, vp, vp, vp]
+        lib.sp_ulysses_step_host.restype = i
         lib.sp_get_device_status.argtypes = [ctypes.c_void_p]
         lib.sp_get_device_status.restype = i
         lib.sp_status_string.argtypes = [i]
@@ -513,6 +532,47 @@ def sp_linear_bwd(dy, x, w, dx=None, dw=None, accumulate_dw: bool = False,
                            n_out, 1 if accumulate_dw else 0, _stream(x.device))
     _check("sp_linear_bwd", rc)
     return dx, dw
+
+
+def sp_ulysses_host_workspace_size(N: int, b: int, s: int, h: int, d: int,
+                                   causal: bool) -> int:
+    return int(load().sp_ulysses_host_workspace_size(N, b, s, h, d, 1 if causal else 0))
+
+
+def sp_ulysses_step_host(q, k, v, dout, o, dq, dk, dv, N: int, causal: bool, workspace,
+                         h2d_stream, d2h_stream, key_len=None, softmax_scale: float = 0.0):
+    """One Ulysses step on page-locked HOST shards [N, b, s/N, h, d] (bf16): o, dq, dk, dv
+    receive the results.  The kernels run on the current stream of the workspace's
+    device, the transfers on h2d_stream and d2h_stream (torch.cuda.Stream)."""
+    lib = load()
+    Nn, b, sl, h, d = q.shape
+    if Nn != N:
+        raise ValueError(f"q has {Nn} shards, N = {N}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout), ("o", o), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if (t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous()
+                or tuple(t.shape) != (N, b, sl, h, d)):
+            raise ValueError(f"{name} must be a contiguous host bf16 tensor of shape "
+                             f"{(N, b, sl, h, d)}")
+    if not workspace.is_cuda or workspace.dtype != torch.uint8:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    p = SpUlyssesHostParams()
+    p.N, p.b, p.s, p.h, p.d = N, b, sl * N, h, d
+    p.causal = 1 if causal else 0
+    p.softmax_scale = float(softmax_scale)
+    if key_len is not None:
+        if key_len.dtype != torch.int32 or not key_len.is_cuda or key_len.numel() != b:
+            raise ValueError("key_len must be a CUDA int32 tensor of b entries")
+        p.key_len = key_len.data_ptr()
+    else:
+        p.key_len = None
+    p.q, p.k, p.v, p.dout = q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr()
+    p.o, p.dq, p.dk, p.dv = o.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    rc = lib.sp_ulysses_step_host(ctypes.byref(p), workspace.data_ptr(), workspace.numel(),
+                                  _stream(workspace.device), h2d_stream.cuda_stream,
+                                  d2h_stream.cuda_stream)
+    _check("sp_ulysses_step_host", rc)
+    return o, dq, dk, dv
 
 
 def sp_get_device_status(device=None) -> int:

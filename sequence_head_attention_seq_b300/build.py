@@ -25,7 +25,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsp.so")
 
 SOURCES = ["sp_abi.cu", "relayout.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_merge.cu",
-           "linear.cu", "attn_bwd_noalloc.cu"]
+           "linear.cu", "attn_bwd_noalloc.cu", "host_step.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

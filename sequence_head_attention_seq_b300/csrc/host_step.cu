@@ -1,0 +1,243 @@
+// host_step.cu -- one Ulysses attention step on HOST-resident shards, with the
+// host<->device traffic overlapped with the attention kernels.
+//
+// The regrouping of "Parallel multi-head attention" section 2.2 and the long-context-
+// attention issue "关于数据分割和合并" (every head group needs its heads from every
+// sequence shard) is, for one head group, a strided gather: N*b runs of s/N rows of
+// (h/N)*d contiguous elements at a pitch of h*d.  A 2-D copy does exactly that, so the
+// copy engines move each head group between the host shard layout and a head-major
+// device buffer while they transfer it, and no relayout kernel runs on this path.
+//
+// Per head group g (slot = g % 2, two slots so that group g+1 moves while g computes):
+//   h2d stream     : Q, K, V of g into the slot            -> qkv_ready[slot]
+//                    dO of g                               -> do_ready[slot]
+//   compute stream : attention forward of g (waits qkv_ready, and out_free of g-2)
+//                                                          -> o_ready[slot]
+//                    attention backward of g (waits do_ready) -> grads_ready[slot]
+//   d2h stream     : O of g to the host (waits o_ready), then dQ, dK, dV (waits
+//                    grads_ready)                          -> out_free[slot]
+// The h2d stream refills a slot only after the backward that last read it
+// (grads_ready of g-2).  Events are created for the call and released at its end
+// (their pending records complete on their own); no device memory is allocated.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace sp {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct HostGeom {
+  int N, b, s, h, d, H, sl;   // H = heads per group, sl = rows per shard
+  size_t elems;               // elements of one group's tensor: b * s * H * d
+};
+
+bool host_geom(int N, int b, int s, int h, int d, HostGeom* g) {
+  if (N < 1 || b < 1 || s < 1 || h < 1 || (d != 64 && d != 128)) return false;
+  if (s % N != 0 || h % N != 0) return false;
+  g->N = N;
+  g->b = b;
+  g->s = s;
+  g->h = h;
+  g->d = d;
+  g->H = h / N;
+  g->sl = s / N;
+  g->elems = static_cast<size_t>(b) * s * g->H * d;
+  return true;
+}
+
+// The attention problem of one head group in its head-major slot buffers [b][s][H][d].
+sp_attn_params group_params(const HostGeom& g, const void* q, const void* k, const void* v,
+                            int causal, const int32_t* key_len, float scale) {
+  sp_attn_params p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  const int64_t st[3] = {static_cast<int64_t>(g.s) * g.H * g.d, static_cast<int64_t>(g.H) * g.d,
+                         g.d};
+  for (int i = 0; i < 3; ++i) p.q_stride[i] = p.k_stride[i] = p.v_stride[i] = p.o_stride[i] = st[i];
+  p.B = g.b;
+  p.H = g.H;
+  p.sq = p.sk = g.s;
+  p.d = g.d;
+  p.causal = causal;
+  p.key_len = key_len;
+  p.softmax_scale = scale;
+  p.seq_shards = 1;
+  return p;
+}
+
+struct Layout {
+  size_t tensor;      // one slot tensor (bf16)
+  size_t lse;         // one slot's lse (fp32 [b][H][s])
+  size_t slot;        // 8 tensors + lse
+  size_t bwd;         // backward workspace, shared by the slots
+  size_t total;
+};
+
+Layout layout_of(const HostGeom& g, int causal) {
+  Layout l;
+  l.tensor = align_up(g.elems * 2);
+  l.lse = align_up(static_cast<size_t>(g.b) * g.H * g.s * 4);
+  l.slot = 8 * l.tensor + l.lse;
+  // only the geometry matters for the size: any 16-byte-aligned stand-in pointer will do
+  const void* stand_in = reinterpret_cast<const void*>(static_cast<uintptr_t>(kAlign));
+  const sp_attn_params p = group_params(g, stand_in, stand_in, stand_in, causal, nullptr, 0.0f);
+  l.bwd = align_up(sp_attn_bwd_workspace_size(&p));
+  l.total = 2 * l.slot + l.bwd;
+  return l;
+}
+
+// Copy head group `grp` of one tensor between the host shard layout [N][b][s/N][h][d]
+// and a head-major device buffer [b][s][H][d].  For b = 1 the shards follow each other
+// at the same host pitch, so one 2-D copy moves the whole group.
+cudaError_t copy_group(const HostGeom& g, int grp, void* host, void* dev, bool to_device,
+                       cudaStream_t st) {
+  const size_t e = 2;   // bf16
+  const size_t width = static_cast<size_t>(g.H) * g.d * e;
+  const size_t hpitch = static_cast<size_t>(g.h) * g.d * e;
+  const int runs_n = g.b == 1 ? 1 : g.N;
+  const int rows = g.b == 1 ? g.s : g.sl;
+  for (int n = 0; n < runs_n; ++n)
+    for (int bb = 0; bb < g.b; ++bb) {
+      // host row (n, bb, 0) and device row (bb, n * s/N)
+      const size_t hrow = (static_cast<size_t>(n) * g.b + bb) * g.sl;
+      const size_t drow = static_cast<size_t>(bb) * g.s + static_cast<size_t>(n) * g.sl;
+      char* hp = static_cast<char*>(host) + hrow * hpitch + static_cast<size_t>(grp) * width;
+      char* dp = static_cast<char*>(dev) + drow * width;
+      const cudaError_t err =
+          to_device ? cudaMemcpy2DAsync(dp, width, hp, hpitch, width, rows, cudaMemcpyHostToDevice, st)
+                    : cudaMemcpy2DAsync(hp, hpitch, dp, width, width, rows, cudaMemcpyDeviceToHost, st);
+      if (err != cudaSuccess) return err;
+    }
+  return cudaSuccess;
+}
+
+bool pinned_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+struct Events {
+  static constexpr int kCount = 12;
+  cudaEvent_t e[kCount] = {};
+  bool create() {
+    for (auto& x : e)
+      if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) return false;
+    return true;
+  }
+  ~Events() {
+    for (auto& x : e)
+      if (x) cudaEventDestroy(x);
+  }
+};
+
+}  // namespace
+}  // namespace sp
+
+using namespace sp;
+
+extern "C" {
+
+size_t sp_ulysses_host_workspace_size(int N, int b, int s, int h, int d, int causal) {
+  HostGeom g;
+  if (!host_geom(N, b, s, h, d, &g) || (causal != 0 && causal != 1)) return 0;
+  const Layout lay = layout_of(g, causal);
+  return lay.bwd == 0 ? 0 : lay.total;
+}
+
+sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
+                               size_t workspace_bytes, void* stream, void* h2d_stream,
+                               void* d2h_stream) {
+  if (p == nullptr) return SP_ERR_INVALID_ARG;
+  HostGeom g;
+  if (p->N < 1 || p->b < 1 || p->s < 1 || p->h < 1 || p->s % p->N != 0 || p->h % p->N != 0 ||
+      (p->causal != 0 && p->causal != 1))
+    return SP_ERR_INVALID_ARG;
+  if (!host_geom(p->N, p->b, p->s, p->h, p->d, &g)) return SP_ERR_UNSUPPORTED;
+  const void* in[4] = {p->q, p->k, p->v, p->dout};
+  void* out[4] = {p->o, p->dq, p->dk, p->dv};
+  for (const void* x : in)
+    if (x == nullptr) return SP_ERR_INVALID_ARG;
+  for (const void* x : out)
+    if (x == nullptr) return SP_ERR_INVALID_ARG;
+  if (workspace == nullptr || h2d_stream == nullptr || d2h_stream == nullptr ||
+      h2d_stream == stream || d2h_stream == stream || h2d_stream == d2h_stream)
+    return SP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return SP_ERR_MISALIGNED;
+  const Layout lay = layout_of(g, p->causal);
+  if (lay.bwd == 0) return SP_ERR_UNSUPPORTED;   // a group problem the kernels refuse
+  if (workspace_bytes < lay.total) return SP_ERR_WORKSPACE;
+  for (const void* x : in)
+    if (!pinned_host(x)) return SP_ERR_INVALID_ARG;
+  for (const void* x : out)
+    if (!pinned_host(x)) return SP_ERR_INVALID_ARG;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStream_t hs = static_cast<cudaStream_t>(h2d_stream);
+  cudaStream_t ds = static_cast<cudaStream_t>(d2h_stream);
+  Events ev;
+  if (!ev.create()) return SP_ERR_CUDA;
+  cudaEvent_t start = ev.e[0], qkv_ready[2] = {ev.e[1], ev.e[2]}, do_ready[2] = {ev.e[3], ev.e[4]},
+              o_ready[2] = {ev.e[5], ev.e[6]}, grads_ready[2] = {ev.e[7], ev.e[8]},
+              out_free[2] = {ev.e[9], ev.e[10]}, done = ev.e[11];
+
+  char* ws = static_cast<char*>(workspace);
+  auto slot_tensor = [&](int slot, int t) { return ws + slot * lay.slot + t * lay.tensor; };
+  auto slot_lse = [&](int slot) { return reinterpret_cast<float*>(ws + slot * lay.slot + 8 * lay.tensor); };
+  void* bwd_ws = ws + 2 * lay.slot;
+
+#define SP_CHECK(x)                            \
+  do {                                         \
+    if ((x) != cudaSuccess) return SP_ERR_CUDA; \
+  } while (0)
+  // the copy streams start after whatever the caller queued before this call
+  SP_CHECK(cudaEventRecord(start, cs));
+  SP_CHECK(cudaStreamWaitEvent(hs, start, 0));
+  SP_CHECK(cudaStreamWaitEvent(ds, start, 0));
+  for (int grp = 0; grp < g.N; ++grp) {
+    const int slot = grp & 1;
+    // slot tensors: 0 q, 1 k, 2 v, 3 dout, 4 o, 5 dq, 6 dk, 7 dv
+    if (grp >= 2) SP_CHECK(cudaStreamWaitEvent(hs, grads_ready[slot], 0));
+    for (int t = 0; t < 3; ++t)
+      SP_CHECK(copy_group(g, grp, const_cast<void*>(in[t]), slot_tensor(slot, t), true, hs));
+    SP_CHECK(cudaEventRecord(qkv_ready[slot], hs));
+    SP_CHECK(copy_group(g, grp, const_cast<void*>(in[3]), slot_tensor(slot, 3), true, hs));
+    SP_CHECK(cudaEventRecord(do_ready[slot], hs));
+
+    SP_CHECK(cudaStreamWaitEvent(cs, qkv_ready[slot], 0));
+    if (grp >= 2) SP_CHECK(cudaStreamWaitEvent(cs, out_free[slot], 0));
+    const sp_attn_params ap = group_params(g, slot_tensor(slot, 0), slot_tensor(slot, 1),
+                                           slot_tensor(slot, 2), p->causal, p->key_len,
+                                           p->softmax_scale);
+    sp_status st = sp_attn_fwd(&ap, slot_tensor(slot, 4), slot_lse(slot), cs);
+    if (st != SP_OK) return st;
+    SP_CHECK(cudaEventRecord(o_ready[slot], cs));
+    SP_CHECK(cudaStreamWaitEvent(cs, do_ready[slot], 0));
+    st = sp_attn_bwd(&ap, slot_tensor(slot, 4), slot_lse(slot), slot_tensor(slot, 3),
+                     slot_tensor(slot, 5), slot_tensor(slot, 6), slot_tensor(slot, 7), bwd_ws,
+                     lay.bwd, cs);
+    if (st != SP_OK) return st;
+    SP_CHECK(cudaEventRecord(grads_ready[slot], cs));
+
+    SP_CHECK(cudaStreamWaitEvent(ds, o_ready[slot], 0));
+    SP_CHECK(copy_group(g, grp, out[0], slot_tensor(slot, 4), false, ds));
+    SP_CHECK(cudaStreamWaitEvent(ds, grads_ready[slot], 0));
+    for (int t = 1; t < 4; ++t) SP_CHECK(copy_group(g, grp, out[t], slot_tensor(slot, 4 + t), false, ds));
+    SP_CHECK(cudaEventRecord(out_free[slot], ds));
+  }
+  // the caller's stream resumes once every result has reached the host
+  SP_CHECK(cudaEventRecord(done, ds));
+  SP_CHECK(cudaStreamWaitEvent(cs, done, 0));
+#undef SP_CHECK
+  return SP_OK;
+}
+
+}  // extern "C"

@@ -17,7 +17,8 @@ import torch
 from .binding import (sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd, sp_attn_merge,
                       sp_linear_bwd, sp_linear_fwd, sp_relayout_head2seq,
                       sp_relayout_head2seq_packed, sp_relayout_seq2head,
-                      sp_relayout_seq2head_packed)
+                      sp_relayout_seq2head_packed, sp_ulysses_host_workspace_size,
+                      sp_ulysses_step_host)
 
 
 class UlyssesAttention:
@@ -141,6 +142,34 @@ class UlyssesAttention:
             self._to_shards((self.dqg, self.dkg, self.dvg), (self.dq, self.dk, self.dv),
                             "head2seq_grads")
         return self.dq, self.dk, self.dv
+
+
+class UlyssesHostStep:
+    """The Ulysses step of UlyssesAttention on page-locked HOST shards [N, b, s/N, h, d]:
+    step() moves the inputs in, runs forward and backward and moves o, dq, dk, dv out,
+    with each head group's transfers overlapping another group's kernels (the copy
+    engines regroup sequence shards into head groups on the way).  Owns the device
+    workspace and the two transfer streams; the kernels run on the current stream."""
+
+    def __init__(self, N, b, s, h, d, causal=True, key_len=None, softmax_scale=0.0,
+                 device=None):
+        device = torch.device(device) if device is not None else torch.device("cuda")
+        self.N, self.causal = N, causal
+        self.softmax_scale = softmax_scale or 0.0
+        # valid keys per batch row, on the device (the same for every head group)
+        self.key_len = (None if key_len is None
+                        else key_len.to(device, torch.int32).contiguous())
+        nbytes = sp_ulysses_host_workspace_size(N, b, s, h, d, causal)
+        if nbytes == 0:
+            raise ValueError("unsupported host-step geometry")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.h2d = torch.cuda.Stream(device)
+        self.d2h = torch.cuda.Stream(device)
+
+    def step(self, q, k, v, dout, o, dq, dk, dv):
+        return sp_ulysses_step_host(q, k, v, dout, o, dq, dk, dv, self.N, self.causal,
+                                    self.workspace, self.h2d, self.d2h, key_len=self.key_len,
+                                    softmax_scale=self.softmax_scale)
 
 
 def _chunk_key_len(key_len, lo, hi):

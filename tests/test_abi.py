@@ -210,3 +210,53 @@ def test_linear_validation(lib):
     assert g(FAKE, FAKE, FAKE, None, None, 4, 64, 64, 0, None) == INVALID   # nothing to do
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 2, None) == INVALID
     assert g(FAKE, FAKE, FAKE, FAKE_ODD, FAKE, 4, 64, 64, 0, None) == MISALIGNED
+
+
+def _host_params(**kw):
+    p = binding.SpUlyssesHostParams()
+    p.N, p.b, p.s, p.h, p.d, p.causal = 2, 1, 256, 4, 64, 1
+    p.q = p.k = p.v = p.dout = p.o = p.dq = p.dk = p.dv = FAKE
+    for name, val in kw.items():
+        setattr(p, name, val)
+    return p
+
+
+def test_host_step_workspace_size(lib):
+    f = lib.sp_ulysses_host_workspace_size
+    # two slots of eight group tensors [b][s][h/N][d] bf16 and the lse, plus the
+    # backward workspace of one group problem (fp32 dQ accumulator + two row statistics)
+    N, b, s, h, d = 2, 1, 256, 4, 64
+    tensor = b * s * (h // N) * d * 2
+    lse = b * (h // N) * s * 4
+    bwd = b * (h // N) * s * d * 4 + 2 * b * (h // N) * s * 4
+    assert f(N, b, s, h, d, 1) == 2 * (8 * tensor + lse) + bwd
+    assert f(0, b, s, h, d, 1) == 0
+    assert f(3, b, s, h, d, 1) == 0            # s % N
+    assert f(N, b, s, 3, d, 1) == 0            # h % N
+    assert f(N, b, s, h, 96, 1) == 0           # head_dim
+    assert f(N, b, s, h, d, 2) == 0            # causal flag
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"N": 0}, INVALID), ({"b": 0}, INVALID), ({"s": 255}, INVALID), ({"h": 3}, INVALID),
+    ({"causal": 2}, INVALID), ({"d": 96}, UNSUPPORTED), ({"q": None}, INVALID),
+    ({"dv": None}, INVALID),
+])
+def test_host_step_validation(lib, kw, code):
+    """Every refusal that needs no GPU: sizes, flags and NULL pointers come first."""
+    big = lib.sp_ulysses_host_workspace_size(2, 1, 256, 4, 64, 1)
+    p = _host_params(**kw)
+    assert lib.sp_ulysses_step_host(ctypes.byref(p), FAKE, big, None, FAKE, FAKE + 16) == code
+
+
+def test_host_step_streams_and_workspace(lib):
+    big = lib.sp_ulysses_host_workspace_size(2, 1, 256, 4, 64, 1)
+    p = _host_params()
+    f = lib.sp_ulysses_step_host
+    assert f(None, FAKE, big, None, FAKE, FAKE + 16) == INVALID
+    assert f(ctypes.byref(p), None, big, None, FAKE, FAKE + 16) == INVALID     # no workspace
+    assert f(ctypes.byref(p), FAKE, big, None, None, FAKE + 16) == INVALID     # no h2d stream
+    assert f(ctypes.byref(p), FAKE, big, None, FAKE, FAKE) == INVALID          # same stream twice
+    assert f(ctypes.byref(p), FAKE, big, FAKE, FAKE, FAKE + 16) == INVALID     # copies on compute
+    assert f(ctypes.byref(p), FAKE + 16, big, None, FAKE, FAKE + 32) == MISALIGNED
+    assert f(ctypes.byref(p), FAKE, big - 1, None, FAKE, FAKE + 16) == WORKSPACE
