@@ -343,6 +343,15 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
                                void* d2h_stream);
 
 /*
+ * Self-test of the failure path that every device-side wait shares: enqueues a
+ * one-warp kernel that waits on an mbarrier nothing arrives on.  The wait gives up
+ * after its limit (2 s), records the timeout in the device status word and the kernel
+ * returns, so the context stays usable; sp_get_device_status then returns
+ * SP_ERR_TIMEOUT (and clears the word).  SP_ERR_CUDA if the launch fails.
+ */
+sp_status sp_selftest_wait_timeout(void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that the
  * kernels set when a bounded device-side wait gives up (SP_ERR_TIMEOUT) or a
  * launch-time invariant fails inside a kernel.  SP_ERR_CUDA if the stream

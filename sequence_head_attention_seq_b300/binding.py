@@ -31,7 +31,7 @@ EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_relayout_seq2head
            "sp_relayout_head2seq_packed", "sp_attn_fwd",
            "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_merge", "sp_linear_fwd",
            "sp_linear_bwd", "sp_attn_bwd_noalloc", "sp_ulysses_host_workspace_size",
-           "sp_ulysses_step_host",
+           "sp_ulysses_step_host", "sp_selftest_wait_timeout",
            "sp_get_device_status", "sp_status_string"]
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024   # SP_NOALLOC_SCRATCH_BYTES
 
@@ -135,6 +135,8 @@ def load(build_if_missing: bool = True):
         lib.sp_ulysses_step_host.argtypes = [ctypes.POINTER(SpUlyssesHostParams), vp,
                                              ctypes.c_size_t, vp, vp, vp]
         lib.sp_ulysses_step_host.restype = i
+        lib.sp_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
+        lib.sp_selftest_wait_timeout.restype = i
         lib.sp_get_device_status.argtypes = [ctypes.c_void_p]
         lib.sp_get_device_status.restype = i
         lib.sp_status_string.argtypes = [i]
@@ -573,6 +575,11 @@ def sp_ulysses_step_host(q, k, v, dout, o, dq, dk, dv, N: int, causal: bool, wor
                                   d2h_stream.cuda_stream)
     _check("sp_ulysses_step_host", rc)
     return o, dq, dk, dv
+
+
+def sp_selftest_wait_timeout(device=None) -> None:
+    """Enqueue the wait-timeout self-test on the current stream (see include/sp.h)."""
+    _check("sp_selftest_wait_timeout", load().sp_selftest_wait_timeout(_stream(device)))
 
 
 def sp_get_device_status(device=None) -> int:

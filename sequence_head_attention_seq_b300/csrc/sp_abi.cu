@@ -251,6 +251,27 @@ Layouts layouts_of(const sp_attn_params* p, const AttnGeom& g) {
 
 using namespace sp;
 
+namespace sp {
+namespace {
+
+// The failure path of every kernel's waits, on its own: one warp waits for phase 0 of an
+// mbarrier that nothing arrives on.  The bounded wait gives up after SP_WAIT_LIMIT_NS,
+// records kStatusTimeout in the status word and the kernel returns normally.
+__global__ void wait_timeout_kernel(uint32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, status, reinterpret_cast<volatile int*>(&abort_flag));
+}
+
+}  // namespace
+}  // namespace sp
+
 extern "C" {
 
 sp_status sp_relayout_seq2head(const void* const* in, void* const* out, int ntensors, int N,
@@ -392,6 +413,13 @@ sp_status sp_attn_merge(const sp_merge_params* p, void* stream) {
   }
   return launch_attn_merge(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SP_OK
                                                                                  : SP_ERR_CUDA;
+}
+
+sp_status sp_selftest_wait_timeout(void* stream) {
+  uint32_t* st = status_word();
+  if (st == nullptr) return SP_ERR_CUDA;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st);
+  return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 
 sp_status sp_get_device_status(void* stream) {
