@@ -58,6 +58,25 @@ def attn_fwd_flops(w) -> float:
     return f / 2 if w.causal else f
 
 
+def valid_pairs(w, key_len=None) -> int:
+    """Exact (query row, key) pairs that take part, summed over batch rows and heads: the
+    causal square counts sum_i (i + 1); padded keys drop out (key j < key_len[b])."""
+    lens = [w.s] * w.b if key_len is None else [int(x) for x in key_len.tolist()]
+    total = 0
+    for n in lens:
+        n = max(0, min(n, w.s))
+        if w.causal:
+            # row i sees keys 0..min(i, n-1)
+            full = min(n, w.s)
+            total += full * (full + 1) // 2 + (w.s - full) * n
+        else:
+            total += w.s * n
+    return total * w.h
+
+
+MUFU_EX2_PER_CLK_SM = 32    # ex2.approx.f32 lanes per clock per SM, measured on B300
+
+
 def step_flops(w) -> float:
     return 3.5 * attn_fwd_flops(w)          # forward + backward (2.5x forward)
 
@@ -450,14 +469,26 @@ def run_ours(args, w):
                     "bytes_per_step": relayout_bytes_per_step(w), "ms_per_step": relayout_ms}
     kernels = {}
     ring_info = None
+    pairs = valid_pairs(w, ins["key_len"])
+    sm_hz = (clock_summary.get("sm_mhz") or 0) * 1e6
     for n, ms in calls.items():
         entry = {"ms": ms}
         if n in ("attn_fwd", "ring_chunk_fwd"):
             entry["ms_per_step"] = per_step[n]
             entry["tflops"] = fwd_f / (per_step[n] * 1e-3) / 1e12
+            # exact work: 4*d flops and one exponential per visible (query, key) pair
+            entry["valid_tflops"] = 4.0 * w.d * pairs / (per_step[n] * 1e-3) / 1e12
+            ex2 = pairs / (per_step[n] * 1e-3)
+            entry["ex2"] = {"per_s": ex2, "unit": "exp/s"}
+            if sm_hz > 0:
+                peak_ex2 = MUFU_EX2_PER_CLK_SM * torch.cuda.get_device_properties(
+                    device).multi_processor_count * sm_hz
+                entry["ex2"].update({"peak": peak_ex2, "frac": ex2 / peak_ex2,
+                                     "peak_basis": "32 lanes/clk/SM x SMs x median SM clock"})
         elif n in ("attn_bwd", "ring_chunk_bwd"):
             entry["ms_per_step"] = per_step[n]
             entry["tflops"] = 2.5 * fwd_f / (per_step[n] * 1e-3) / 1e12
+            entry["valid_tflops"] = 10.0 * w.d * pairs / (per_step[n] * 1e-3) / 1e12
         elif n.startswith("proj_"):
             M, dim, hd = w.b * w.s, w.h * w.d, w.h * w.d
             f = 2.0 * M * dim * (3 * hd if "qkv" in n else hd) * (2 if n.endswith("_bwd") else 1)

@@ -72,6 +72,25 @@ sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int nten
                                int N, int b, int s, int h, int d, void* stream);
 
 /*
+ * The regrouping in the form of the sequence-parallel all-to-all of transformers PR
+ * 31525 ("Support deepspeed sequence parallel"): every rank's tensor is 4-D, one
+ * dimension is split across the N ranks (scatter_dim) and another is concatenated
+ * from them (gather_dim).  On one GPU the N ranks' tensors are stacked along a leading
+ * dimension of size N, in and out.
+ *
+ *   shape          : the per-rank INPUT shape [b][x][y][d] (4 entries, each >= 1)
+ *   scatter 2, gather 1 : in [N][b][s/N][h][d] -> out [N][b][s][h/N][d]  (x = s/N, y = h;
+ *                         the same as sp_relayout_seq2head with one tensor)
+ *   scatter 1, gather 2 : in [N][b][s][h/N][d] -> out [N][b][s/N][h][d]  (x = s, y = h/N;
+ *                         the same as sp_relayout_head2seq with one tensor)
+ * Other (scatter_dim, gather_dim) pairs -> SP_ERR_UNSUPPORTED.  A NULL shape, an entry
+ * below 1 or N < 1 -> SP_ERR_INVALID_ARG; otherwise arguments and errors as
+ * sp_relayout_seq2head.
+ */
+sp_status sp_relayout(const void* in, void* out, int N, const int64_t shape[4], int scatter_dim,
+                      int gather_dim, void* stream);
+
+/*
  * Packed Q/K/V (the long-context-attention issue names a packed-QKV variant of its
  * attention, LongContextAttentionQKVPacked): one sequence-shard buffer holding all
  * three, [N][b][s/N][3][h][d], regrouped into three head-group buffers in one launch.

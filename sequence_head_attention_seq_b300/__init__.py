@@ -4,6 +4,7 @@ The computation lives in ``libsp.so`` (C ABI in ``include/sp.h``, CUDA kernels i
 ``csrc/``).  This package is its thin binding:
 
     sp_relayout_seq2head / sp_relayout_head2seq   sequence shards <-> head groups
+    sp_relayout                                   the same as an all-to-all (scatter/gather dims)
     sp_attn_fwd                                   attention forward (out + lse)
     sp_attn_bwd                                   attention backward (dq, dk, dv)
     sp_attn_merge                                 ring / blockwise: merge key-chunk results
@@ -18,7 +19,7 @@ calls raise.
 """
 from .binding import (SpError, sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_fwd,
                       sp_attn_merge, sp_get_device_status, sp_linear_bwd, sp_linear_fwd,
-                      sp_relayout_head2seq,
+                      sp_relayout, sp_relayout_head2seq,
                       sp_relayout_head2seq_packed, sp_relayout_seq2head,
                       sp_relayout_seq2head_packed, sp_status_string,
                       sp_ulysses_host_workspace_size, sp_ulysses_step_host)
@@ -26,7 +27,7 @@ from .pipeline import (AttentionLayer, UlyssesAttention, UlyssesHostStep, ring_a
                        ring_attention_fwd)
 
 __all__ = ["SpError", "sp_attn_bwd", "sp_attn_bwd_workspace_size", "sp_attn_fwd", "sp_attn_merge",
-           "sp_get_device_status", "sp_relayout_head2seq", "sp_relayout_seq2head",
+           "sp_get_device_status", "sp_relayout", "sp_relayout_head2seq", "sp_relayout_seq2head",
            "sp_relayout_seq2head_packed", "sp_relayout_head2seq_packed", "sp_linear_fwd",
            "sp_linear_bwd",
            "sp_status_string", "sp_ulysses_host_workspace_size", "sp_ulysses_step_host",

@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED",
 MAX_RELAYOUT_TENSORS = 8
 
 # Every symbol include/sp.h declares.
-EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_relayout_seq2head_packed",
+EXPORTS = ["sp_relayout_seq2head", "sp_relayout_head2seq", "sp_relayout", "sp_relayout_seq2head_packed",
            "sp_relayout_head2seq_packed", "sp_attn_fwd",
            "sp_attn_bwd_workspace_size", "sp_attn_bwd", "sp_attn_merge", "sp_linear_fwd",
            "sp_linear_bwd", "sp_attn_bwd_noalloc", "sp_ulysses_host_workspace_size",
@@ -108,6 +108,9 @@ def load(build_if_missing: bool = True):
             f = getattr(lib, name)
             f.argtypes = [vpp, vpp, i, i, i, i, i, i, ctypes.c_void_p]
             f.restype = i
+        lib.sp_relayout.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i,
+                                    ctypes.POINTER(ctypes.c_int64), i, i, ctypes.c_void_p]
+        lib.sp_relayout.restype = i
         lib.sp_relayout_seq2head_packed.argtypes = [ctypes.c_void_p, vpp, i, i, i, i, i,
                                                     ctypes.c_void_p]
         lib.sp_relayout_seq2head_packed.restype = i
@@ -212,6 +215,29 @@ def sp_relayout_head2seq(inputs, N: int, outs=None):
         raise ValueError("s must be divisible by N")
     return _relayout("sp_relayout_head2seq", inputs, N, b, s, hl * N, d,
                      (N, b, s // N, hl * N, d), outs)
+
+
+def sp_relayout(x, N: int, scatter_dim: int, gather_dim: int, out=None):
+    """The all-to-all in scatter/gather form on N stacked per-rank tensors [N][b][x][y][d]:
+    (2, 1) is sequence shards -> head groups, (1, 2) head groups -> sequence shards."""
+    lib = load()
+    _need_bf16_cuda("x", x)
+    if x.dim() != 5 or x.shape[0] != N or not x.is_contiguous():
+        raise ValueError("expected N contiguous per-rank tensors [N][b][x][y][d]")
+    _, b, xd, yd, d = x.shape
+    if (scatter_dim, gather_dim) == (2, 1):
+        oshape = (N, b, xd * N, yd // N, d)
+    elif (scatter_dim, gather_dim) == (1, 2):
+        oshape = (N, b, xd // N, yd * N, d)
+    else:
+        oshape = tuple(x.shape)
+    if out is None:
+        out = torch.empty(oshape, dtype=x.dtype, device=x.device)
+    shape = (ctypes.c_int64 * 4)(b, xd, yd, d)
+    rc = lib.sp_relayout(x.data_ptr(), out.data_ptr(), N, shape, scatter_dim, gather_dim,
+                         _stream(x.device))
+    _check("sp_relayout", rc)
+    return out
 
 
 def _same_layout(a: torch.Tensor, b: torch.Tensor) -> bool:

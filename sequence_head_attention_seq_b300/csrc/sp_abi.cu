@@ -284,6 +284,32 @@ sp_status sp_relayout_head2seq(const void* const* in, void* const* out, int nten
   return relayout(in, out, ntensors, N, b, s, h, d, false, stream);
 }
 
+sp_status sp_relayout(const void* in, void* out, int N, const int64_t shape[4], int scatter_dim,
+                      int gather_dim, void* stream) {
+  if (shape == nullptr) return SP_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (shape[i] < 1 || shape[i] > INT32_MAX) return SP_ERR_INVALID_ARG;
+  if (N < 1) return SP_ERR_INVALID_ARG;
+  const int b = static_cast<int>(shape[0]), d = static_cast<int>(shape[3]);
+  const void* src[1] = {in};
+  void* dst[1] = {out};
+  if (scatter_dim == 2 && gather_dim == 1) {
+    // per-rank input [b][s/N][h][d]: heads scattered, sequence gathered
+    const int64_t s = shape[1] * N;
+    if (s > INT32_MAX) return SP_ERR_INVALID_ARG;
+    return relayout(src, dst, 1, N, b, static_cast<int>(s), static_cast<int>(shape[2]), d, true,
+                    stream);
+  }
+  if (scatter_dim == 1 && gather_dim == 2) {
+    // per-rank input [b][s][h/N][d]: sequence scattered, heads gathered
+    const int64_t h = shape[2] * N;
+    if (h > INT32_MAX) return SP_ERR_INVALID_ARG;
+    return relayout(src, dst, 1, N, b, static_cast<int>(shape[1]), static_cast<int>(h), d, false,
+                    stream);
+  }
+  return SP_ERR_UNSUPPORTED;
+}
+
 sp_status sp_relayout_seq2head_packed(const void* qkv, void* const* out, int N, int b, int s,
                                       int h, int d, void* stream) {
   if (h < 1 || d < 1) return SP_ERR_INVALID_ARG;

@@ -260,3 +260,18 @@ def test_host_step_streams_and_workspace(lib):
     assert f(ctypes.byref(p), FAKE, big, FAKE, FAKE, FAKE + 16) == INVALID     # copies on compute
     assert f(ctypes.byref(p), FAKE + 16, big, None, FAKE, FAKE + 32) == MISALIGNED
     assert f(ctypes.byref(p), FAKE, big - 1, None, FAKE, FAKE + 16) == WORKSPACE
+
+
+def test_general_relayout_validation(lib):
+    f = lib.sp_relayout
+    shape = (ctypes.c_int64 * 4)(1, 8, 4, 64)
+    assert f(FAKE, FAKE * 2, 2, None, 2, 1, None) == INVALID           # no shape
+    assert f(FAKE, FAKE * 2, 0, shape, 2, 1, None) == INVALID          # N < 1
+    assert f(FAKE, FAKE * 2, 2, shape, 0, 3, None) == UNSUPPORTED      # other dims
+    assert f(FAKE, FAKE * 2, 2, shape, 2, 2, None) == UNSUPPORTED
+    assert f(FAKE, FAKE * 2, 3, shape, 2, 1, None) == INVALID          # h = 4 not split by 3
+    assert f(FAKE, FAKE * 2, 3, shape, 1, 2, None) == INVALID          # s = 8 not split by 3
+    bad = (ctypes.c_int64 * 4)(1, 0, 4, 64)
+    assert f(FAKE, FAKE * 2, 2, bad, 2, 1, None) == INVALID            # an empty dimension
+    assert f(None, FAKE * 2, 2, shape, 2, 1, None) == INVALID
+    assert f(FAKE_ODD, FAKE * 2, 2, shape, 2, 1, None) == MISALIGNED

@@ -1,0 +1,33 @@
+"""Host-side accounting of bench.py: the exact count of visible (query, key) pairs that
+the valid-work figures divide by, against brute force."""
+import itertools
+import os
+import sys
+
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+from sequence_head_attention_seq_b300 import workloads  # noqa: E402
+
+
+def _brute(s, b, h, causal, lens):
+    return h * sum(1 for bb, i, j in itertools.product(range(b), range(s), range(s))
+                   if (not causal or j <= i) and j < lens[bb])
+
+
+@pytest.mark.parametrize("s,b,h,causal,lens", [
+    (7, 1, 2, True, None), (7, 2, 3, False, None), (9, 3, 1, True, [4, 9, 0]),
+    (9, 2, 2, False, [1, 8]), (6, 2, 1, True, [12, -3]),
+])
+def test_valid_pairs_brute_force(s, b, h, causal, lens):
+    w = workloads.Workload("t", 1, b=b, h=h, d=64, s=s, N=1, causal=causal, scale=1.0)
+    kl = None if lens is None else torch.tensor(lens)
+    want = _brute(s, b, h, causal, [max(0, min(n, s)) for n in (lens or [s] * b)])
+    assert bench.valid_pairs(w, kl) == want
+
+
+def test_valid_pairs_dense_causal_closed_form():
+    w = workloads.WORKLOADS["llama70b"]
+    assert bench.valid_pairs(w) == w.b * w.h * w.s * (w.s + 1) // 2

@@ -105,3 +105,20 @@ def test_packed_relayout_matches_oracle(N, b, s, h, d):
         part = qkv[:, :, :, t].contiguous()
         assert np.array_equal(u16(groups[t]), orc.seq2head(u16(part), N, b, s, h, d)), t
     assert np.array_equal(u16(back), u16(qkv))
+
+
+@pytest.mark.parametrize("N,b,s,h,d", [(2, 1, 128, 2, 64), (4, 2, 64, 8, 128), (3, 2, 12, 6, 8)])
+def test_all_to_all_form_matches_oracle(N, b, s, h, d):
+    """sp_relayout with (scatter 2, gather 1) and (scatter 1, gather 2): the oracle's
+    index loop, bit for bit, and the inverse of each other."""
+    need_gpu()
+    from sequence_head_attention_seq_b300 import sp_relayout
+    orc = oracle.default()
+    x = _rand_bits((N, b, s // N, h, d), 300 + N)
+    g = sp_relayout(x, N, 2, 1)
+    y = sp_relayout(g, N, 1, 2)
+    torch.cuda.synchronize()
+    check_status()
+    assert tuple(g.shape) == (N, b, s, h // N, d)
+    assert np.array_equal(u16(g), orc.seq2head(u16(x), N, b, s, h, d))
+    assert np.array_equal(u16(y), u16(x))
