@@ -145,6 +145,21 @@ def test_empty_rows():
     assert not dq[0].any() and not dk[0].any() and not dv[0].any()
 
 
+def test_out_of_range_key_len_is_clamped():
+    """A length below 0 hides every key and one above sk hides none: the results are
+    those of [0, sk], bit for bit (dq within the gradient bar)."""
+    need_gpu()
+    q, do = _randn((2, 130, 1, 64), 96), _randn((2, 130, 1, 64), 97)
+    k, v = _randn((2, 140, 1, 64), 98), _randn((2, 140, 1, 64), 99)
+    a = _run(q, k, v, do, False, key_len=[-3, 190])
+    b = _run(q, k, v, do, False, key_len=[0, 140])
+    for name, x, y in zip(("o", "lse", "dk", "dv"), (a[0], a[1], a[3], a[4]),
+                          (b[0], b[1], b[3], b[4])):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y), name
+    check_grad(f64(a[2]), f64(b[2]), "dq")
+
+
 def test_repeat_calls_are_deterministic_forward():
     need_gpu()
     q, k, v = (_randn((1, 700, 3, 128), 95 + t) for t in range(3))
