@@ -30,6 +30,19 @@ struct AttnGeom {
   float scale_log2;           // scale * log2(e)
 };
 
+// CTA -> (batch entry x head, work class) for a launch of `heads` x `classes` CTAs in
+// groups of `group` heads: within a group, class 0 (the heaviest) of every head first.
+__device__ __forceinline__ void cta_order(int cta, int heads, int classes, int group, int* bh,
+                                          int* cls) {
+  const int per_group = group * classes;
+  const int g = cta / per_group;
+  const int r = cta - g * per_group;
+  const int gs = min(group, heads - g * group);
+  const int c = r / gs;
+  *cls = c;
+  *bh = g * group + (r - c * gs);
+}
+
 // Rows of the per-head statistics arrays in the backward workspace (sq rounded to 128).
 inline int64_t padded_rows(int sq) { return (static_cast<int64_t>(sq) + 127) / 128 * 128; }
 
