@@ -30,17 +30,21 @@ struct AttnGeom {
   float scale_log2;           // scale * log2(e)
 };
 
-// CTA -> (batch entry x head, work class) for a launch of `heads` x `classes` CTAs in
-// groups of `group` heads: within a group, class 0 (the heaviest) of every head first.
-__device__ __forceinline__ void cta_order(int cta, int heads, int classes, int group, int* bh,
-                                          int* cls) {
-  const int per_group = group * classes;
+// log2 of the largest power of two that divides `heads` and is at most `cap` (0 when cap
+// < 2): a group size with no partial last group.
+int group_shift(int64_t heads, int64_t cap);
+// L2 bytes of the current device (0 if unknown), queried once per device.
+int64_t device_l2_bytes();
+
+// CTA -> (batch entry x head, work class) for a launch of heads x `classes` CTAs in groups
+// of 2^gshift heads (which divides the head count): within a group, class 0 (the
+// heaviest) of every head first.
+__device__ __forceinline__ void cta_order(int cta, int classes, int gshift, int* bh, int* cls) {
+  const int per_group = classes << gshift;
   const int g = cta / per_group;
   const int r = cta - g * per_group;
-  const int gs = min(group, heads - g * group);
-  const int c = r / gs;
-  *cls = c;
-  *bh = g * group + (r - c * gs);
+  *cls = r >> gshift;
+  *bh = (g << gshift) + (r & ((1 << gshift) - 1));
 }
 
 // Rows of the per-head statistics arrays in the backward workspace (sq rounded to 128).

@@ -272,6 +272,31 @@ __global__ void wait_timeout_kernel(uint32_t* status) {
 }  // namespace
 }  // namespace sp
 
+namespace sp {
+
+int group_shift(int64_t heads, int64_t cap) {
+  int shift = 0;
+  while ((int64_t(2) << shift) <= cap && heads % (int64_t(2) << shift) == 0) ++shift;
+  return shift;
+}
+
+int64_t device_l2_bytes() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int64_t> cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  int64_t l2 = cache[dev].load(std::memory_order_relaxed);
+  if (l2 == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) return 0;
+    l2 = v;
+    cache[dev].store(l2, std::memory_order_relaxed);
+  }
+  return l2;
+}
+
+}  // namespace sp
+
 extern "C" {
 
 sp_status sp_relayout_seq2head(const void* const* in, void* const* out, int ntensors, int N,
