@@ -280,7 +280,7 @@ sp_status sp_linear_bwd(const void* dy, const void* x, const void* w, void* dx, 
 /*
  * sp_attn_bwd for callers that cannot allocate device memory: code running inside a
  * framework or runtime that owns all device memory (no cudaMalloc/cudaFree allowed on
- * its threads), or code bound to a fixed memory plan.  The paper has no counterpart.
+ * its threads), or code bound to a fixed memory plan.  None of the cited pages has one.
  *
  * Instead of a caller-supplied workspace it uses a library-owned device array of
  * SP_NOALLOC_SCRATCH_BYTES, created on every GPU that loads the library and kept

@@ -9,7 +9,7 @@
 // point below allocates nothing.  The array is created when the library's
 // device code is loaded on a GPU and stays there until the process exits.
 //
-// The paper has no counterpart: this is a packaging variant of sp_attn_bwd.
+// None of the cited pages has a counterpart: this is a packaging variant of sp_attn_bwd.
 #include <atomic>
 
 #include "internal.h"
