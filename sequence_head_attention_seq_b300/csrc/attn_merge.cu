@@ -13,7 +13,8 @@
 // the first chunk) and 4 written, plus 2 bytes of o_out on the last chunk.  One thread
 // moves 8 consecutive head-dim elements (16-byte bf16 and 32-byte fp32 vectors);
 // the d/8 threads of one row sit in the same warp, which lets one of them update the
-// row's lse after all of them have read the old value.
+// row's lse after all of them have read the old value.  All loads are issued before
+// any arithmetic, so each thread waits for memory once.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -35,8 +36,20 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const MergeArgs a) {
   const int64_t lse_at = (static_cast<int64_t>(bb) * a.H + h) * a.sq + i;
   float lse_new = -INFINITY;
   if (active) {
-    const float lp = a.lse_part[lse_at];
+    // every load first (they do not depend on each other), so that a thread waits for
+    // memory once rather than for the statistics and then for the accumulator
+    const float lp = __ldg(a.lse_part + lse_at);
     const float la = a.init ? -INFINITY : a.lse_acc[lse_at];
+    const uint4 part = __ldg(reinterpret_cast<const uint4*>(
+        static_cast<const __nv_bfloat16*>(a.o_part) + bb * a.part_stride[0] +
+        static_cast<int64_t>(i) * a.part_stride[1] + h * a.part_stride[2] + c * 8));
+    float4* acc = reinterpret_cast<float4*>(a.o_acc + ((static_cast<int64_t>(bb) * a.sq + i) *
+                                                           a.H + h) * D + c * 8);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+    if (!a.init) {   // uniform across the launch
+      x = acc[0];
+      y = acc[1];
+    }
     const float m = fmaxf(lp, la);
     float wa = 0.0f, wp = 0.0f;
     if (m != -INFINITY) {
@@ -46,29 +59,16 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const MergeArgs a) {
       wa = ea / sum;
       wp = ep / sum;
     }
-    const uint4 part = *reinterpret_cast<const uint4*>(
-        static_cast<const __nv_bfloat16*>(a.o_part) + bb * a.part_stride[0] +
-        static_cast<int64_t>(i) * a.part_stride[1] + h * a.part_stride[2] + c * 8);
+    // a side with weight 0 is left out (not multiplied by 0): the accumulator of a
+    // row that has seen no key yet is never used, whatever it holds
     const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&part);
+    const float xa[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
     float o[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 f = __bfloat1622float2(p2[k]);
-      o[2 * k] = wp * f.x;
-      o[2 * k + 1] = wp * f.y;
-    }
-    float4* acc = reinterpret_cast<float4*>(a.o_acc + ((static_cast<int64_t>(bb) * a.sq + i) *
-                                                           a.H + h) * D + c * 8);
-    if (!a.init && wa != 0.0f) {
-      const float4 x = acc[0], y = acc[1];
-      o[0] = fmaf(wa, x.x, o[0]);
-      o[1] = fmaf(wa, x.y, o[1]);
-      o[2] = fmaf(wa, x.z, o[2]);
-      o[3] = fmaf(wa, x.w, o[3]);
-      o[4] = fmaf(wa, y.x, o[4]);
-      o[5] = fmaf(wa, y.y, o[5]);
-      o[6] = fmaf(wa, y.z, o[6]);
-      o[7] = fmaf(wa, y.w, o[7]);
+      o[2 * k] = wa != 0.0f ? fmaf(wa, xa[2 * k], wp * f.x) : wp * f.x;
+      o[2 * k + 1] = wa != 0.0f ? fmaf(wa, xa[2 * k + 1], wp * f.y) : wp * f.y;
     }
     acc[0] = make_float4(o[0], o[1], o[2], o[3]);
     acc[1] = make_float4(o[4], o[5], o[6], o[7]);
