@@ -60,55 +60,75 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        float* __restrict__ stats,
                                                        float* __restrict__ dq_acc, int B, int H,
                                                        int sq, int64_t rows) {
-  // one warp per (batch entry, head, padded row)
+  // one warp per kRowsPerWarp consecutive (batch entry, head, padded row) rows: all of
+  // their loads are issued before any reduction, so that a warp waits for memory once
+  constexpr int kRowsPerWarp = 4;
+  constexpr int kPer = D / 32;   // elements per lane
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   const int64_t total = static_cast<int64_t>(B) * H * rows;
-  if (wid >= total) return;
-  const int64_t i = wid % rows;
-  const int64_t bh = wid / rows;
+  const int64_t first = wid * kRowsPerWarp;
+  if (first >= total) return;
+  // rows is a multiple of 128, so the kRowsPerWarp rows share one (batch entry, head)
+  const int64_t bh = first / rows;
+  const int64_t i0 = first % rows;
   const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
-  constexpr int kPer = D / 32;   // elements per lane
-  float acc = 0.0f;
-  if (i < sq) {
-    const int64_t off = ao.off(b, static_cast<int>(i), h) + lane * kPer;
-    if constexpr (kPer == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-      const uint2 c = *reinterpret_cast<const uint2*>(dout + off);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+  float x[kRowsPerWarp][kPer], y[kRowsPerWarp][kPer];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float2 x = __bfloat1622float2(a2[k]);
-        const float2 y = __bfloat1622float2(c2[k]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) x[r][k] = y[r][k] = 0.0f;
+    const int64_t i = i0 + r;
+    if (i < sq) {
+      const int64_t off = ao.off(b, static_cast<int>(i), h) + lane * kPer;
+      if constexpr (kPer == 4) {
+        const uint2 a2 = *reinterpret_cast<const uint2*>(o + off);
+        const uint2 c2 = *reinterpret_cast<const uint2*>(dout + off);
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a2);
+        const __nv_bfloat162* pc = reinterpret_cast<const __nv_bfloat162*>(&c2);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float2 fa = __bfloat1622float2(pa[k]), fc = __bfloat1622float2(pc[k]);
+          x[r][2 * k] = fa.x;
+          x[r][2 * k + 1] = fa.y;
+          y[r][2 * k] = fc.x;
+          y[r][2 * k + 1] = fc.y;
+        }
+      } else {
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + off));
+        const float2 fc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + off));
+        x[r][0] = fa.x;
+        x[r][1] = fa.y;
+        y[r][0] = fc.x;
+        y[r][1] = fc.y;
       }
-    } else {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + off);
-      const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(dout + off);
-      const float2 x = __bfloat1622float2(a);
-      const float2 y = __bfloat1622float2(c);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   float* srow = stats + bh * 2 * rows;
-  if (lane == 0) {
-    float nl2 = -INFINITY;   // padded or empty row: P = exp2(x - inf) = 0
-    if (i < sq) {
-      const float v = lse[bh * sq + i];
-      if (v != -INFINITY) nl2 = -v * kLog2e;
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc = fmaf(x[r][k], y[r][k], acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const int64_t i = i0 + r;
+    if (lane == 0) {
+      float nl2 = -INFINITY;   // padded or empty row: P = exp2(x - inf) = 0
+      if (i < sq) {
+        const float v = lse[bh * sq + i];
+        if (v != -INFINITY) nl2 = -v * kLog2e;
+      }
+      srow[i] = nl2;
+      srow[rows + i] = (i < sq) ? acc : 0.0f;
     }
-    srow[i] = nl2;
-    srow[rows + i] = (i < sq) ? acc : 0.0f;
   }
   if (dq_acc != nullptr) {   // null: keep the previous call's accumulator
-    float4* z = reinterpret_cast<float4*>(dq_acc + (bh * rows + i) * D);
+    // the kRowsPerWarp rows are contiguous in the accumulator
+    float4* z = reinterpret_cast<float4*>(dq_acc + (bh * rows + i0) * D);
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = lane; c < D / 4; c += 32) z[c] = zero;
+#pragma unroll
+    for (int c = lane; c < kRowsPerWarp * D / 4; c += 32) z[c] = zero;
   }
 }
 
@@ -671,7 +691,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   // 1. statistics + zero the dQ accumulator; a call that continues an accumulation
   //    over key chunks reuses both (same o, lse and dout as the previous call)
   if (!a.dq_accumulate) {
-    const int64_t warps = bh * rows;
+    const int64_t warps = bh * rows / 4;   // four rows per warp (rows is a multiple of 128)
     const int64_t blocks = (warps * 32 + 255) / 256;
     if (blocks > 0) {
       if (g.d == 128)
