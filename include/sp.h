@@ -310,7 +310,9 @@ sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o, const floa
  * s/N rows of (h/N)*d elements at a pitch of h*d; one copy when b = 1) between the host
  * shard layout and a head-major device buffer, and back for the results.  Group g's
  * copies in, its forward and backward on `stream`, and its copies out run on three
- * streams with group g+1's transfers overlapping group g's kernels (two buffer slots).
+ * streams with group g+1's transfers overlapping group g's kernels (two buffer slots);
+ * the first and the last group go as two halves of their heads, which halves the
+ * transfers that no kernel can hide.
  *
  * The results equal those of sp_relayout_seq2head, sp_attn_fwd, sp_relayout_head2seq,
  * sp_relayout_seq2head (dout), sp_attn_bwd and sp_relayout_head2seq on the same data:

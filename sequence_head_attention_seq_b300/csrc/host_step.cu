@@ -17,9 +17,13 @@
 //   d2h stream     : O of g to the host (waits o_ready), then dQ, dK, dV (waits
 //                    grads_ready)                          -> out_free[slot]
 // The h2d stream refills a slot only after the backward that last read it
-// (grads_ready of g-2).  Events are created for the call and released at its end
+// (grads_ready of g-2).  The first and the last head group go as two halves of their
+// heads: only the first unit's inputs and the last unit's results are not overlapped
+// with kernels, so halving those units halves the exposed transfer time.  Events are created for the call and released at its end
 // (their pending records complete on their own); no device memory is allocated.
 #include <cuda_runtime.h>
+
+#include <vector>
 
 #include "internal.h"
 
@@ -49,18 +53,19 @@ bool host_geom(int N, int b, int s, int h, int d, HostGeom* g) {
   return true;
 }
 
-// The attention problem of one head group in its head-major slot buffers [b][s][H][d].
-sp_attn_params group_params(const HostGeom& g, const void* q, const void* k, const void* v,
-                            int causal, const int32_t* key_len, float scale) {
+// The attention problem of `nh` heads of one head group in their head-major slot
+// buffers [b][s][nh][d].
+sp_attn_params group_params(const HostGeom& g, int nh, const void* q, const void* k,
+                            const void* v, int causal, const int32_t* key_len, float scale) {
   sp_attn_params p{};
   p.q = q;
   p.k = k;
   p.v = v;
-  const int64_t st[3] = {static_cast<int64_t>(g.s) * g.H * g.d, static_cast<int64_t>(g.H) * g.d,
+  const int64_t st[3] = {static_cast<int64_t>(g.s) * nh * g.d, static_cast<int64_t>(nh) * g.d,
                          g.d};
   for (int i = 0; i < 3; ++i) p.q_stride[i] = p.k_stride[i] = p.v_stride[i] = p.o_stride[i] = st[i];
   p.B = g.b;
-  p.H = g.H;
+  p.H = nh;
   p.sq = p.sk = g.s;
   p.d = g.d;
   p.causal = causal;
@@ -85,19 +90,25 @@ Layout layout_of(const HostGeom& g, int causal) {
   l.slot = 8 * l.tensor + l.lse;
   // only the geometry matters for the size: any 16-byte-aligned stand-in pointer will do
   const void* stand_in = reinterpret_cast<const void*>(static_cast<uintptr_t>(kAlign));
-  const sp_attn_params p = group_params(g, stand_in, stand_in, stand_in, causal, nullptr, 0.0f);
+  const sp_attn_params p = group_params(g, g.H, stand_in, stand_in, stand_in, causal, nullptr,
+                                       0.0f);
   l.bwd = align_up(sp_attn_bwd_workspace_size(&p));
   l.total = 2 * l.slot + l.bwd;
   return l;
 }
 
-// Copy head group `grp` of one tensor between the host shard layout [N][b][s/N][h][d]
-// and a head-major device buffer [b][s][H][d].  For b = 1 the shards follow each other
-// at the same host pitch, so one 2-D copy moves the whole group.
-cudaError_t copy_group(const HostGeom& g, int grp, void* host, void* dev, bool to_device,
-                       cudaStream_t st) {
+// A unit of work: heads j0 .. j0+nh-1 of head group grp.
+struct Unit {
+  int grp, j0, nh;
+};
+
+// Copy one unit of one tensor between the host shard layout [N][b][s/N][h][d] and a
+// head-major device buffer [b][s][nh][d].  For b = 1 the shards follow each other at
+// the same host pitch, so one 2-D copy moves the whole unit.
+cudaError_t copy_unit(const HostGeom& g, const Unit& u, void* host, void* dev, bool to_device,
+                      cudaStream_t st) {
   const size_t e = 2;   // bf16
-  const size_t width = static_cast<size_t>(g.H) * g.d * e;
+  const size_t width = static_cast<size_t>(u.nh) * g.d * e;
   const size_t hpitch = static_cast<size_t>(g.h) * g.d * e;
   const int runs_n = g.b == 1 ? 1 : g.N;
   const int rows = g.b == 1 ? g.s : g.sl;
@@ -106,7 +117,8 @@ cudaError_t copy_group(const HostGeom& g, int grp, void* host, void* dev, bool t
       // host row (n, bb, 0) and device row (bb, n * s/N)
       const size_t hrow = (static_cast<size_t>(n) * g.b + bb) * g.sl;
       const size_t drow = static_cast<size_t>(bb) * g.s + static_cast<size_t>(n) * g.sl;
-      char* hp = static_cast<char*>(host) + hrow * hpitch + static_cast<size_t>(grp) * width;
+      char* hp = static_cast<char*>(host) + hrow * hpitch +
+                 (static_cast<size_t>(u.grp) * g.H + u.j0) * g.d * e;
       char* dp = static_cast<char*>(dev) + drow * width;
       const cudaError_t err =
           to_device ? cudaMemcpy2DAsync(dp, width, hp, hpitch, width, rows, cudaMemcpyHostToDevice, st)
@@ -202,19 +214,32 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
   SP_CHECK(cudaEventRecord(start, cs));
   SP_CHECK(cudaStreamWaitEvent(hs, start, 0));
   SP_CHECK(cudaStreamWaitEvent(ds, start, 0));
+  // the first and the last head group in two halves of their heads
+  std::vector<Unit> units;
+  const int half = g.H / 2;
   for (int grp = 0; grp < g.N; ++grp) {
-    const int slot = grp & 1;
+    if (half > 0 && (grp == 0 || grp == g.N - 1)) {
+      units.push_back({grp, 0, half});
+      units.push_back({grp, half, g.H - half});
+      if (g.N == 1) break;
+    } else {
+      units.push_back({grp, 0, g.H});
+    }
+  }
+  for (size_t ui = 0; ui < units.size(); ++ui) {
+    const Unit& u = units[ui];
+    const int slot = static_cast<int>(ui & 1);
     // slot tensors: 0 q, 1 k, 2 v, 3 dout, 4 o, 5 dq, 6 dk, 7 dv
-    if (grp >= 2) SP_CHECK(cudaStreamWaitEvent(hs, grads_ready[slot], 0));
+    if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(hs, grads_ready[slot], 0));
     for (int t = 0; t < 3; ++t)
-      SP_CHECK(copy_group(g, grp, const_cast<void*>(in[t]), slot_tensor(slot, t), true, hs));
+      SP_CHECK(copy_unit(g, u, const_cast<void*>(in[t]), slot_tensor(slot, t), true, hs));
     SP_CHECK(cudaEventRecord(qkv_ready[slot], hs));
-    SP_CHECK(copy_group(g, grp, const_cast<void*>(in[3]), slot_tensor(slot, 3), true, hs));
+    SP_CHECK(copy_unit(g, u, const_cast<void*>(in[3]), slot_tensor(slot, 3), true, hs));
     SP_CHECK(cudaEventRecord(do_ready[slot], hs));
 
     SP_CHECK(cudaStreamWaitEvent(cs, qkv_ready[slot], 0));
-    if (grp >= 2) SP_CHECK(cudaStreamWaitEvent(cs, out_free[slot], 0));
-    const sp_attn_params ap = group_params(g, slot_tensor(slot, 0), slot_tensor(slot, 1),
+    if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(cs, out_free[slot], 0));
+    const sp_attn_params ap = group_params(g, u.nh, slot_tensor(slot, 0), slot_tensor(slot, 1),
                                            slot_tensor(slot, 2), p->causal, p->key_len,
                                            p->softmax_scale);
     sp_status st = sp_attn_fwd(&ap, slot_tensor(slot, 4), slot_lse(slot), cs);
@@ -228,9 +253,10 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
     SP_CHECK(cudaEventRecord(grads_ready[slot], cs));
 
     SP_CHECK(cudaStreamWaitEvent(ds, o_ready[slot], 0));
-    SP_CHECK(copy_group(g, grp, out[0], slot_tensor(slot, 4), false, ds));
+    SP_CHECK(copy_unit(g, u, out[0], slot_tensor(slot, 4), false, ds));
     SP_CHECK(cudaStreamWaitEvent(ds, grads_ready[slot], 0));
-    for (int t = 1; t < 4; ++t) SP_CHECK(copy_group(g, grp, out[t], slot_tensor(slot, 4 + t), false, ds));
+    for (int t = 1; t < 4; ++t)
+      SP_CHECK(copy_unit(g, u, out[t], slot_tensor(slot, 4 + t), false, ds));
     SP_CHECK(cudaEventRecord(out_free[slot], ds));
   }
   // the caller's stream resumes once every result has reached the host
