@@ -228,6 +228,7 @@ def oracle_sample(w, heads: int, prefix: int):
     drawn with the workload's seeds and scale (a bounded sample of the same problem)."""
     import oracle
     orc = oracle.default()
+    heads, prefix = min(heads, w.h), min(prefix, w.s)
     shape = (1, prefix, heads, w.d)
     q = workloads.randn_bf16(shape, w.seed("q"), w.scale).double().numpy()
     k = workloads.randn_bf16(shape, w.seed("k"), w.scale).double().numpy()
@@ -238,11 +239,11 @@ def oracle_sample(w, heads: int, prefix: int):
     orc.attn_bwd(q, k, v, do, w.causal)
     dt = time.perf_counter() - t0
     flops = 3.5 * 4.0 * heads * prefix * prefix * w.d / (2 if w.causal else 1)
-    return flops, dt, orc.threads()
+    return flops, dt, orc.threads(), heads, prefix
 
 
 def cpu_baseline(w, heads=4, prefix=8192):
-    flops, dt, cores = oracle_sample(w, heads, prefix)
+    flops, dt, cores, heads, prefix = oracle_sample(w, heads, prefix)
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"fp64 C oracle, causal fwd+bwd of {heads} heads over the first {prefix} "
                       f"positions of {w.name} (d={w.d}); {flops / 1e9:.1f} GFLOP in {dt:.1f} s"}
@@ -259,7 +260,7 @@ def run_reference(args, w):
         oracle_sample(w, heads, prefix)
     total_flops, total_t, cores = 0.0, 0.0, 1
     for _ in range(args.steps):
-        f, dt, cores = oracle_sample(w, heads, prefix)
+        f, dt, cores, heads, prefix = oracle_sample(w, heads, prefix)
         total_flops += f
         total_t += dt
     value = total_flops / total_t / 1e12
@@ -278,12 +279,22 @@ def run_reference(args, w):
     return 0
 
 
+def l2_note(w) -> str:
+    """Whether a step's data outruns L2 between timed steps: a step reads and writes the
+    eight shard tensors and their eight head-group copies."""
+    ws = 16 * tensor_bytes(w)
+    per = f"{tensor_bytes(w) / 2**20:.0f} MiB per tensor, {ws / 2**20:.0f} MiB touched per step"
+    if ws > 126e6:
+        return f"inputs larger than L2 ({per}, 126 MB L2)"
+    return f"working set within the 126 MB L2 ({per}); not flushed between steps"
+
+
 def config_of(w, ring_chunks: int = 0):
     extra = {"ring_chunks": ring_chunks} if ring_chunks > 1 else {}
     return {**extra, "workload": w.name, "b": w.b, "heads": w.h, "head_dim": w.d, "seq_len": w.s,
             "sp_degree": w.N, "heads_per_group": w.h_local, "causal": w.causal,
             "input_scale": w.scale,
-            "l2": f"inputs larger than L2 ({tensor_bytes(w) / 2**20:.0f} MiB per tensor, 126 MB L2)",
+            "l2": l2_note(w),
             "flops_convention": "fwd 4*b*h*s^2*d/2 (causal), bwd 2.5x fwd"}
 
 

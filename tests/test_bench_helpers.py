@@ -31,3 +31,27 @@ def test_valid_pairs_brute_force(s, b, h, causal, lens):
 def test_valid_pairs_dense_causal_closed_form():
     w = workloads.WORKLOADS["llama70b"]
     assert bench.valid_pairs(w) == w.b * w.h * w.s * (w.s + 1) // 2
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores) prints one JSON line
+    with the keys the benchmark contract names; it needs no GPU."""
+    import json
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                          "tiny", "--steps", "1", "--warmup", "3"], cwd=root,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 1
+    assert line["config"]["workload"] == "tiny"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert "first 128 positions" in cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
