@@ -244,9 +244,22 @@ def oracle_sample(w, heads: int, prefix: int):
 
 def cpu_baseline(w, heads=4, prefix=8192):
     flops, dt, cores, heads, prefix = oracle_sample(w, heads, prefix)
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+    line = {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"fp64 C oracle, causal fwd+bwd of {heads} heads over the first {prefix} "
                       f"positions of {w.name} (d={w.d}); {flops / 1e9:.1f} GFLOP in {dt:.1f} s"}
+    # the same oracle on one core, on a smaller sample of the same problem
+    import oracle
+    orc = oracle.default()
+    threads = orc.threads()
+    orc.set_threads(1)
+    try:
+        f1, dt1, _, h1, p1 = oracle_sample(w, 1, 2048)
+    finally:
+        orc.set_threads(threads)
+    line["single_core"] = {"value": f1 / dt1 / 1e12, "unit": UNIT, "cores": 1,
+                           "sample": f"1 head over the first {p1} positions; "
+                                     f"{f1 / 1e9:.1f} GFLOP in {dt1:.1f} s"}
+    return line
 
 
 # ---------------------------------------------------------------- arms
