@@ -24,6 +24,11 @@ SHAPES = [
                        scale=1.0, key_len_range=(700, 2048)),
     # b = 1: one 2-D copy per tensor and head group
     workloads.WORKLOADS["llama7b"],
+    # one shard: the single head group goes as two halves of its heads
+    workloads.Workload("host_one_shard", 95, b=1, h=4, d=128, s=384, N=1, causal=True,
+                       scale=1.0),
+    # one head per group: no group can be split
+    workloads.Workload("host_one_head", 96, b=1, h=2, d=64, s=512, N=2, causal=True, scale=1.0),
 ]
 
 
