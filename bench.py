@@ -114,10 +114,15 @@ def load_peaks():
 
 
 def source_digest(names) -> str:
+    """sha256 (16 hex digits) of the kernel sources' code: comments and white space are
+    removed first, so a change of wording leaves it alone and a change of code does not."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "sequence_head_attention_seq_b300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "sequence_head_attention_seq_b300", "csrc", n)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(re.sub(r"\s+", "", text).encode())
     return h.hexdigest()[:16]
 
 

@@ -216,9 +216,10 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
 // Per query tile i the MMA thread issues
 //   (dQ_{i-1} read out) dP^T_i | (P^T_i half h in TMEM) dV += P^T_h dO_h, h = 0, 1 |
 //   S^T_{i+1} | (dS_i in shared memory) dQ_i, dK += dS^T Q_i
-// and each warpgroup, per tile, computes P from S^T (while dP^T runs), writes P^T and
-// signals it, then computes dS from dP^T (while dV and the next S^T run), then reads
-// dQ_i out of TMEM and adds it to the accumulator (while dK runs).  The tensor core thus
+// Each compute warpgroup, per tile, computes P from S^T (while dP^T runs), writes P^T and
+// signals it, then computes dS from dP^T (while dV and the next S^T run); the drain
+// warpgroup reads dQ_i out of TMEM (while dK runs), which frees the columns for the next
+// dP^T, and adds it to the accumulator while the next tile proceeds.  The tensor core thus
 // works on one product or another while the warpgroups compute, instead of waiting for
 // both halves of P and dS before any dV, dK or next-tile product can start.  The next
 // S^T overwrites the P^T columns only after the dV products that read them (tcgen05 MMAs
