@@ -426,6 +426,37 @@ def run_ours(args, w):
     flops = step_flops(w) + (proj_flops(w) if args.layer else 0.0)
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
+    # the same step captured once in a CUDA graph and replayed (no per-call host launch
+    # cost); reported beside the eager number, which stays the headline
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            one_step()                       # settles any first-call setup off the capture
+            side.synchronize()
+            with torch.cuda.graph(cg, stream=side):
+                one_step()
+        torch.cuda.current_stream(device).wait_stream(side)
+        for _ in range(args.warmup):
+            cg.replay()
+        torch.cuda.synchronize()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            cg.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        barrier()
+        if sp_get_device_status() != 0:
+            raise RuntimeError("device status reported an error during graph replay")
+        gms = reduce_max(g0.elapsed_time(g1), device) / args.steps
+        graph = {"value": world * flops / (gms * 1e-3) / 1e12, "unit": UNIT,
+                 "ms_per_step": gms}
+        del cg
+
     # end to end through the public API: pinned host buffers in, results back out
     e2e = None
     if not args.no_e2e and not args.layer:
@@ -559,6 +590,7 @@ def run_ours(args, w):
         "kernels": kernels,
         "ring": ring_info,
         "e2e": e2e,
+        **({"graph": graph} if graph is not None else {}),
         "gpu_launches": launches_per_step(w, args.ring, args.fused) * args.steps,
         "clocks": clock_summary,
     }
@@ -591,6 +623,8 @@ def main(argv=None):
     ap.add_argument("--key-mask", action="store_true",
                     help="give the workload's key padding as a general per-key mask "
                          "(the mask path of the kernels) instead of key lengths")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph and replayed")
     ap.add_argument("--heads", type=int, default=None,
                     help="total heads instead of the workload's (same sequence, head dim and "
                          "shard count; for profiling a smaller case of the same kernels)")
