@@ -184,6 +184,8 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
       h2d_stream == stream || d2h_stream == stream || h2d_stream == d2h_stream)
     return SP_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return SP_ERR_MISALIGNED;
+  // key lengths are int32: checked here so that nothing is queued before a refusal
+  if ((reinterpret_cast<uintptr_t>(p->key_len) & 3u) != 0) return SP_ERR_MISALIGNED;
   const Layout lay = layout_of(g, p->causal);
   if (lay.bwd == 0) return SP_ERR_UNSUPPORTED;   // a group problem the kernels refuse
   if (workspace_bytes < lay.total) return SP_ERR_WORKSPACE;

@@ -259,6 +259,8 @@ def test_host_step_streams_and_workspace(lib):
     assert f(ctypes.byref(p), FAKE, big, None, FAKE, FAKE) == INVALID          # same stream twice
     assert f(ctypes.byref(p), FAKE, big, FAKE, FAKE, FAKE + 16) == INVALID     # copies on compute
     assert f(ctypes.byref(p), FAKE + 16, big, None, FAKE, FAKE + 32) == MISALIGNED
+    pk = _host_params(key_len=FAKE + 2)
+    assert f(ctypes.byref(pk), FAKE, big, None, FAKE, FAKE + 16) == MISALIGNED  # key_len
     assert f(ctypes.byref(p), FAKE, big - 1, None, FAKE, FAKE + 16) == WORKSPACE
 
 
