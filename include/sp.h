@@ -338,7 +338,8 @@ sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o, const floa
  * Errors: N, b, s, h < 1, s % N or h % N != 0, causal not 0/1, a NULL pointer or
  *         stream, repeated streams, a host pointer that is not page-locked host memory
  *         -> SP_ERR_INVALID_ARG; d not 64/128 -> SP_ERR_UNSUPPORTED; workspace too
- *         small -> SP_ERR_WORKSPACE, misaligned -> SP_ERR_MISALIGNED; a failed CUDA
+ *         small -> SP_ERR_WORKSPACE; workspace or key_len misaligned ->
+ *         SP_ERR_MISALIGNED; all of these before anything is queued.  A failed CUDA
  *         call -> SP_ERR_CUDA (work already queued by this call then still runs).
  */
 typedef struct sp_ulysses_host_params {
