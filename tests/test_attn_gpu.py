@@ -275,10 +275,30 @@ def _check_tiny_split_q(w, ins):
     check_grad(dvs.double().cpu().numpy(), rdv, "tiny split-Q dv sum")
 
 
+def _head_tensors(step, gi, j):
+    """q, k, v, dout of head j of head group gi as [1][s][1][d] fp64 (the oracle's layout)."""
+    return [t[gi, 0, :, j, :].double().cpu().numpy()[None, :, None, :]
+            for t in (step.qg, step.kg, step.vg, step.dog)]
+
+
+# Key blocks whose dK/dV are compared with the oracle on the long workloads.  Under the
+# causal mask key block 0 is seen by every query row and key block s/2 by half of them,
+# so these are the longest loops of the backward (every query tile accumulated into the
+# same dK/dV columns); the last block is its shortest loop.
+def _key_blocks(w, sampled_head):
+    first, middle, last = (0, 128), (w.s // 2, w.s // 2 + 128), (w.s - 256, w.s)
+    if w.s <= 32768:
+        return [first, middle, last]
+    # 131072 tokens: every extra block costs the oracle a forward over the rows that see
+    # it (minutes), so each sampled head takes one of the two long blocks
+    return [first, last] if sampled_head == 0 else [middle, last]
+
+
 @pytest.mark.parametrize("name,ring", [("llama70b", 0), ("ulysses131k", 0), ("llama70b", 8)])
 def test_workload_sampled_rows(name, ring):
-    """Long workloads: sampled query rows (out, lse, dq) and the last key rows (dk, dv)
-    of sampled heads against the oracle, plus the gradient-sum properties on every head.
+    """Long workloads: sampled query rows (out, lse, dq) and whole key blocks (dk, dv) at
+    the start, the middle and the end of the sequence, for sampled heads, against the
+    oracle; plus the gradient-sum properties on every head.
     ring > 1: the same step with attention run blockwise over that many key chunks."""
     need_gpu()
     w = workloads.WORKLOADS[name]
@@ -294,11 +314,11 @@ def test_workload_sampled_rows(name, ring):
         again = sp_relayout_head2seq([g_t], w.N)[0]
         assert torch.equal(again.view(torch.int16), s_t.view(torch.int16))
     orc = oracle.default()
-    rows = [0, 1, 127, 128, w.s // 2 + 5, w.s - 129, w.s - 1]
-    keys = (w.s - 256, w.s)
-    for gi, j in ((0, 0), (w.N - 1, w.h_local - 1)):
-        tensors = [t[gi, 0, :, j, :].double().cpu().numpy()[None, :, None, :]
-                   for t in (step.qg, step.kg, step.vg, step.dog)]
+    # rows of the first, second, middle and last query tiles
+    rows = [0, 1, 5, 63, 127, 128, 200, 255, w.s // 2, w.s // 2 + 5, w.s // 2 + 127,
+            w.s - 129, w.s - 64, w.s - 1]
+    for sampled, (gi, j) in enumerate(((0, 0), (w.N - 1, w.h_local - 1))):
+        tensors = _head_tensors(step, gi, j)
         tag = f"{name} group {gi} head {j}"
         for i in rows:
             ro, rl = orc.attn_fwd_rows(*tensors[:3], 0, 0, i, i + 1, True)
@@ -311,7 +331,48 @@ def test_workload_sampled_rows(name, ring):
             dq_ref.append(rdq)
             dq_gpu.append(step.dqg[gi, 0, i, j].double().cpu().numpy()[None])
         check_grad(np.concatenate(dq_gpu), np.concatenate(dq_ref), f"{tag} dq rows")
-        _, rdk, rdv = orc.attn_bwd_rows(*tensors, 0, 0, 0, 0, keys[0], keys[1], True)
-        check_grad(step.dkg[gi, 0, keys[0]:keys[1], j].double().cpu().numpy(), rdk, f"{tag} dk rows")
-        check_grad(step.dvg[gi, 0, keys[0]:keys[1], j].double().cpu().numpy(), rdv, f"{tag} dv rows")
+        for j0, j1 in _key_blocks(w, sampled):
+            _, rdk, rdv = orc.attn_bwd_rows(*tensors, 0, 0, 0, 0, j0, j1, True)
+            check_grad(step.dkg[gi, 0, j0:j1, j].double().cpu().numpy(), rdk,
+                       f"{tag} dk keys {j0}..{j1}")
+            check_grad(step.dvg[gi, 0, j0:j1, j].double().cpu().numpy(), rdv,
+                       f"{tag} dv keys {j0}..{j1}")
     _check_gradient_sums(step, w, ins["dout"])
+
+
+@pytest.mark.slow
+def test_llama70b_whole_head():
+    """One whole head of the LLaMA-70B-shaped step (32768 positions, d = 128) against the
+    oracle over every row and every key: out, lse, dq, dk, dv at the bars of the small
+    cases.  Heads are independent, so this covers the kernels' full-length loops (every
+    key block up to 256 query tiles, every query row up to 32768 keys) element by element.
+    The oracle's part is about a minute on 16 host cores."""
+    need_gpu()
+    w = workloads.WORKLOADS["llama70b"]
+    ins = workloads.make_inputs(w, device="cuda")
+    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal)
+    step.forward(ins["q"], ins["k"], ins["v"])
+    step.backward(ins["dout"])
+    torch.cuda.synchronize()
+    check_status()
+    gi, j = w.N // 2, w.h_local // 2 - 1       # a head in the middle of the middle group
+    tensors = _head_tensors(step, gi, j)
+    got = {n: getattr(step, n)[gi, 0, :, j].double().cpu().numpy()
+           for n in ("og", "dqg", "dkg", "dvg")}
+    got_lse = step.lse[gi * w.b, j].double().cpu().numpy()
+    del step, ins
+    torch.cuda.empty_cache()
+    orc = oracle.default()
+    ro, rl = orc.attn_fwd_rows(*tensors[:3], 0, 0, 0, w.s, True)
+    check_out(got["og"], ro, "whole head out")
+    check_lse(got_lse, rl, "whole head lse")
+    rdq, rdk, rdv = orc.attn_bwd_rows(*tensors, 0, 0, 0, w.s, 0, w.s, True)
+    check_grad(got["dqg"], rdq, "whole head dq")
+    check_grad(got["dkg"], rdk, "whole head dk")
+    check_grad(got["dvg"], rdv, "whole head dv")
+    # and per 128-key block, so that no block hides behind the norm of the others
+    for j0 in range(0, w.s, 128):
+        check_grad(got["dkg"][j0:j0 + 128], rdk[j0:j0 + 128], f"whole head dk keys {j0}..")
+        check_grad(got["dvg"][j0:j0 + 128], rdv[j0:j0 + 128], f"whole head dv keys {j0}..")
+    for i0 in range(0, w.s, 128):
+        check_grad(got["dqg"][i0:i0 + 128], rdq[i0:i0 + 128], f"whole head dq rows {i0}..")
