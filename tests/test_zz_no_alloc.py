@@ -11,6 +11,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from gpu_util import check_grad, check_status, f64, need_gpu
 from sequence_head_attention_seq_b300 import binding, sp_attn_bwd, sp_attn_fwd, workloads
 
@@ -36,13 +37,22 @@ def test_noalloc_matches_workspace_backward_twice(B, H, sq, sk, d, causal, key_l
     ref = sp_attn_bwd(q, k, v, o, lse, do, causal, 0, kl)
     torch.cuda.synchronize()
     check_status()
+    orc = oracle.default()
+    want = orc.attn_bwd(f64(q), f64(k), f64(v), f64(do), causal, 0, key_len)
     # two calls in a row: the second one finds the first one's leftovers in the scratch
     for call in range(2):
         got = binding.sp_attn_bwd_noalloc(q, k, v, o, lse, do, causal, 0, kl)
         torch.cuda.synchronize()
         check_status()
-        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
-            check_grad(f64(a), f64(b), f"call {call} {name}")
+        # the same kernels run in the same order on the same inputs: dK and dV come out
+        # of per-CTA accumulators and must be identical bit for bit; dQ is a sum of
+        # atomically added fp32 pieces whose order may differ from run to run
+        for name, a, b in zip(("dk", "dv"), got[1:], ref[1:]):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
+                f"call {call} {name} differs from sp_attn_bwd"
+        check_grad(f64(got[0]), f64(ref[0]), f"call {call} dq vs sp_attn_bwd")
+        for name, a, r in zip(("dq", "dk", "dv"), got, want):
+            check_grad(f64(a), r, f"call {call} {name} vs oracle")
 
 
 @pytest.mark.gpu
