@@ -312,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
+  int q_issued = 0;   // producer: query tiles whose Q, statistics and dO loads were issued
 
   // Every CTA takes the same register split, whatever work it has; each warpgroup sets
   // its limit at the top of its own branch.
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       for (int c = 0; c < kChunks; ++c)
         tma_load_5d(sm.dout[s] + c * 16384, &p.tdo, &sm.do_full[s], c * 64, rq.head, rq.row,
                     rq.batch, rq.shard);
+      q_issued = it + 1;
     }
   } else if (warp == 1 && lane == 0 && nq > 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -444,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     }
     mma_commit(&sm.dkv_full);
     if (!ok) {
+      // unwinding: let every issued MMA finish before TMEM is released
       mma_commit(&sm.drain);
-      int never = 0;
-      mbar_wait(&sm.drain, 0, p.status, &never);
+      mbar_wait_settle(&sm.drain, 0, p.status);
     }
   }
   } else if (warp < 12) {
@@ -678,6 +680,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  if (warp == 0 && lane == 0 && nq > 0 && *abort_flag) {
+    // unwinding: shared memory stays with this CTA until the loads already issued into
+    // it have landed (every armed phase had all of its loads issued)
+    mbar_wait_settle(&sm.kv_full, 0, p.status);
+    for (int s = 0; s < 2; ++s) {
+      const int armed = ring_phases(q_issued, s, 2);
+      if (armed > 0) {
+        mbar_wait_settle(&sm.q_full[s], (armed - 1) & 1, p.status);
+        mbar_wait_settle(&sm.do_full[s], (armed - 1) & 1, p.status);
+      }
+    }
   }
 }
 

@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
+  int kv_issued = 0;   // producer: key blocks whose K and V loads were issued
 
   if (warp == 0 && lane == 0 && nmax > 0) {
     // ------------------------------------------------------------ TMA producer
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int c = 0; c < kChunks; ++c)
         tma_load_5d(sm.v[s] + c * 16384, &p.tv, &sm.v_full[s], c * 64, r.head, r.row, r.batch,
                     r.shard);
+      kv_issued = n + 1;
     }
   } else if (warp == 1 && lane == 0 && nmax > 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -270,8 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (!ok) {
       // unwinding: let every issued MMA finish before TMEM is released
       mma_commit(&sm.drain);
-      int never = 0;
-      mbar_wait(&sm.drain, 0, p.status, &never);
+      mbar_wait_settle(&sm.drain, 0, p.status);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
@@ -439,6 +440,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  if (warp == 0 && lane == 0 && nmax > 0 && *abort_flag) {
+    // unwinding: shared memory stays with this CTA until the loads already issued into
+    // it have landed (every armed phase had all of its loads issued)
+    mbar_wait_settle(&sm.q_full, 0, p.status);
+    for (int s = 0; s < kStages; ++s) {
+      const int armed = ring_phases(kv_issued, s, kStages);
+      if (armed > 0) {
+        mbar_wait_settle(&sm.k_full[s], (armed - 1) & 1, p.status);
+        mbar_wait_settle(&sm.v_full[s], (armed - 1) & 1, p.status);
+      }
+    }
   }
 }
 

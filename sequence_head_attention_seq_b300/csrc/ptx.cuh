@@ -103,6 +103,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
+// Wait for a barrier phase that work already in flight completes by itself (TMA copies
+// that were issued, MMAs that were committed), while a CTA unwinds after giving up: the
+// CTA must not exit, and its TMEM must not be freed, while such work still writes or
+// reads them.  Bounded by time alone (the abort flag and the status word are already
+// set); false, with a timeout recorded, if the phase is still open after the limit.
+__device__ __forceinline__ bool mbar_wait_settle(uint64_t* bar, uint32_t parity,
+                                                 uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > SP_WAIT_LIMIT_NS) {
+      raise_status(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Phases armed so far on stage `s` of a `stages`-deep ring after `issued` uses in
+// order (use n goes to stage n % stages).
+__device__ __forceinline__ int ring_phases(int issued, int s, int stages) {
+  return issued > s ? (issued - 1 - s) / stages + 1 : 0;
+}
+
 // ---------------------------------------------------------------- fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
