@@ -291,8 +291,10 @@ sp_status sp_linear_bwd(const void* dy, const void* x, const void* w, void* dx, 
  *    SP_NOALLOC_SCRATCH_BYTES are rejected with SP_ERR_WORKSPACE before any launch.
  *  - dq_accumulate must be 0 (SP_ERR_INVALID_ARG otherwise): the shared scratch does
  *    not carry an accumulation from one call to the next.
- *  - The first call on each device looks up the array's device address (with that
- *    device current); make that first call before capturing any stream.
+ *  - Every CUDA context that loads the library holds its own copy of the array (the
+ *    device's primary context, or a caller's own driver-API context).  The first call
+ *    in a context looks up the array's device address with that context current and
+ *    caches it per context; make that first call before capturing any stream.
  *  - All calls share the one array per device and it keeps whatever the last call
  *    left in it (every byte is rewritten before it is read, so nothing needs
  *    clearing).  Calls whose kernels overlap on the GPU (different streams without
@@ -340,7 +342,11 @@ sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o, const floa
  *         -> SP_ERR_INVALID_ARG; d not 64/128 -> SP_ERR_UNSUPPORTED; workspace too
  *         small -> SP_ERR_WORKSPACE; workspace or key_len misaligned ->
  *         SP_ERR_MISALIGNED; all of these before anything is queued.  A failed CUDA
- *         call -> SP_ERR_CUDA (work already queued by this call then still runs).
+ *         call or a refusal by a kernel entry point part-way -> its status (SP_ERR_CUDA
+ *         for a failed CUDA call); copies already queued by this call then still run,
+ *         and `stream` is made to wait for both transfer streams before the call
+ *         returns, so synchronising `stream` is enough before the host buffers are
+ *         freed or reused.
  */
 typedef struct sp_ulysses_host_params {
     int N, b, s, h, d;        /* shards, batch rows, full sequence, heads, head_dim */

@@ -10,8 +10,6 @@
 // device code is loaded on a GPU and stays there until the process exits.
 //
 // None of the cited pages has a counterpart: this is a packaging variant of sp_attn_bwd.
-#include <atomic>
-
 #include "internal.h"
 
 // Scratch for sp_attn_bwd_noalloc.  In host code this name is only a host-side
@@ -22,21 +20,17 @@ static __device__ __align__(256) uint8_t g_bwd_scratch[SP_NOALLOC_SCRATCH_BYTES]
 namespace sp {
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+ContextAddressCache g_scratch_addr;
 
-// Device address of g_bwd_scratch on the current device, looked up once per device.
+// Device address of g_bwd_scratch in the current CUDA context.  The first call in a
+// context (normally the device's primary context; a caller's own driver-API context gets
+// its own copy of the array) looks it up with cudaGetSymbolAddress, with that context
+// current; later calls reuse the cached address.
 void* scratch_address() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  void* a = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (a == nullptr) {
+  return g_scratch_addr.get([]() -> void* {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return nullptr;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
-    a = p;
-  }
-  return a;
+    return cudaGetSymbolAddress(&p, g_bwd_scratch) == cudaSuccess ? p : nullptr;
+  });
 }
 
 }  // namespace

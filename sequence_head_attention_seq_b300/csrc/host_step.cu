@@ -228,38 +228,51 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
       units.push_back({grp, 0, g.H});
     }
   }
-  for (size_t ui = 0; ui < units.size(); ++ui) {
-    const Unit& u = units[ui];
-    const int slot = static_cast<int>(ui & 1);
-    // slot tensors: 0 q, 1 k, 2 v, 3 dout, 4 o, 5 dq, 6 dk, 7 dv
-    if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(hs, grads_ready[slot], 0));
-    for (int t = 0; t < 3; ++t)
-      SP_CHECK(copy_unit(g, u, const_cast<void*>(in[t]), slot_tensor(slot, t), true, hs));
-    SP_CHECK(cudaEventRecord(qkv_ready[slot], hs));
-    SP_CHECK(copy_unit(g, u, const_cast<void*>(in[3]), slot_tensor(slot, 3), true, hs));
-    SP_CHECK(cudaEventRecord(do_ready[slot], hs));
+  // Queue every unit.  A failure part-way leaves copies queued on hs and ds: the
+  // caller's stream is then joined to both before the error is returned, so that
+  // synchronising the caller's stream also waits for every copy that touches the host
+  // buffers (the caller may free or reuse them after that).
+  auto enqueue_units = [&]() -> sp_status {
+    for (size_t ui = 0; ui < units.size(); ++ui) {
+      const Unit& u = units[ui];
+      const int slot = static_cast<int>(ui & 1);
+      // slot tensors: 0 q, 1 k, 2 v, 3 dout, 4 o, 5 dq, 6 dk, 7 dv
+      if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(hs, grads_ready[slot], 0));
+      for (int t = 0; t < 3; ++t)
+        SP_CHECK(copy_unit(g, u, const_cast<void*>(in[t]), slot_tensor(slot, t), true, hs));
+      SP_CHECK(cudaEventRecord(qkv_ready[slot], hs));
+      SP_CHECK(copy_unit(g, u, const_cast<void*>(in[3]), slot_tensor(slot, 3), true, hs));
+      SP_CHECK(cudaEventRecord(do_ready[slot], hs));
 
-    SP_CHECK(cudaStreamWaitEvent(cs, qkv_ready[slot], 0));
-    if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(cs, out_free[slot], 0));
-    const sp_attn_params ap = group_params(g, u.nh, slot_tensor(slot, 0), slot_tensor(slot, 1),
-                                           slot_tensor(slot, 2), p->causal, p->key_len,
-                                           p->softmax_scale);
-    sp_status st = sp_attn_fwd(&ap, slot_tensor(slot, 4), slot_lse(slot), cs);
-    if (st != SP_OK) return st;
-    SP_CHECK(cudaEventRecord(o_ready[slot], cs));
-    SP_CHECK(cudaStreamWaitEvent(cs, do_ready[slot], 0));
-    st = sp_attn_bwd(&ap, slot_tensor(slot, 4), slot_lse(slot), slot_tensor(slot, 3),
-                     slot_tensor(slot, 5), slot_tensor(slot, 6), slot_tensor(slot, 7), bwd_ws,
-                     lay.bwd, cs);
-    if (st != SP_OK) return st;
-    SP_CHECK(cudaEventRecord(grads_ready[slot], cs));
+      SP_CHECK(cudaStreamWaitEvent(cs, qkv_ready[slot], 0));
+      if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(cs, out_free[slot], 0));
+      const sp_attn_params ap = group_params(g, u.nh, slot_tensor(slot, 0), slot_tensor(slot, 1),
+                                             slot_tensor(slot, 2), p->causal, p->key_len,
+                                             p->softmax_scale);
+      sp_status st = sp_attn_fwd(&ap, slot_tensor(slot, 4), slot_lse(slot), cs);
+      if (st != SP_OK) return st;
+      SP_CHECK(cudaEventRecord(o_ready[slot], cs));
+      SP_CHECK(cudaStreamWaitEvent(cs, do_ready[slot], 0));
+      st = sp_attn_bwd(&ap, slot_tensor(slot, 4), slot_lse(slot), slot_tensor(slot, 3),
+                       slot_tensor(slot, 5), slot_tensor(slot, 6), slot_tensor(slot, 7), bwd_ws,
+                       lay.bwd, cs);
+      if (st != SP_OK) return st;
+      SP_CHECK(cudaEventRecord(grads_ready[slot], cs));
 
-    SP_CHECK(cudaStreamWaitEvent(ds, o_ready[slot], 0));
-    SP_CHECK(copy_unit(g, u, out[0], slot_tensor(slot, 4), false, ds));
-    SP_CHECK(cudaStreamWaitEvent(ds, grads_ready[slot], 0));
-    for (int t = 1; t < 4; ++t)
-      SP_CHECK(copy_unit(g, u, out[t], slot_tensor(slot, 4 + t), false, ds));
-    SP_CHECK(cudaEventRecord(out_free[slot], ds));
+      SP_CHECK(cudaStreamWaitEvent(ds, o_ready[slot], 0));
+      SP_CHECK(copy_unit(g, u, out[0], slot_tensor(slot, 4), false, ds));
+      SP_CHECK(cudaStreamWaitEvent(ds, grads_ready[slot], 0));
+      for (int t = 1; t < 4; ++t)
+        SP_CHECK(copy_unit(g, u, out[t], slot_tensor(slot, 4 + t), false, ds));
+      SP_CHECK(cudaEventRecord(out_free[slot], ds));
+    }
+    return SP_OK;
+  };
+  const sp_status queued = enqueue_units();
+  if (queued != SP_OK) {
+    if (cudaEventRecord(qkv_ready[0], hs) == cudaSuccess) cudaStreamWaitEvent(cs, qkv_ready[0], 0);
+    if (cudaEventRecord(done, ds) == cudaSuccess) cudaStreamWaitEvent(cs, done, 0);
+    return queued;
   }
   // the caller's stream resumes once every result has reached the host
   SP_CHECK(cudaEventRecord(done, ds));

@@ -4,10 +4,45 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <mutex>
 
 #include "sp.h"
 
 namespace sp {
+
+// The calling thread's current CUDA context (the device's primary context when the
+// runtime made it current), or null when none is current or the driver is unreachable.
+void* current_context();
+
+// Device address of one of the library's __device__ variables, cached per CUDA
+// context: every context that loads the library holds its own copy of each such
+// variable, so an address looked up in one context is not valid in another (a caller
+// may run in its own driver-API context instead of the device's primary one).
+// `lookup` runs with the context current and returns the address (null on failure).
+class ContextAddressCache {
+ public:
+  template <class Lookup>
+  void* get(Lookup lookup) {
+    void* ctx = current_context();
+    if (ctx == nullptr) return nullptr;
+    std::lock_guard<std::mutex> lock(mu_);
+    for (int i = 0; i < n_; ++i)
+      if (entries_[i].ctx == ctx) return entries_[i].addr;
+    void* addr = lookup();
+    if (addr != nullptr && n_ < kEntries) entries_[n_++] = Entry{ctx, addr};
+    return addr;
+  }
+
+ private:
+  static constexpr int kEntries = 256;
+  struct Entry {
+    void* ctx;
+    void* addr;
+  };
+  std::mutex mu_;
+  Entry entries_[kEntries];
+  int n_ = 0;
+};
 
 constexpr int kMaxRelayoutTensors = SP_MAX_RELAYOUT_TENSORS;
 

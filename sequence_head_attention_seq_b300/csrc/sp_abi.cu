@@ -20,21 +20,14 @@ __device__ uint32_t g_device_status;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::atomic<uint32_t*> g_status_addr[kMaxDevices];
+ContextAddressCache g_status_addr;
 
-// Device address of the status word for the current device (looked up once per device).
+// Device address of the status word in the current context (looked up once per context).
 uint32_t* status_word() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  uint32_t* a = g_status_addr[dev].load(std::memory_order_acquire);
-  if (a == nullptr) {
+  return static_cast<uint32_t*>(g_status_addr.get([]() -> void* {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    a = static_cast<uint32_t*>(p);
-    g_status_addr[dev].store(a, std::memory_order_release);
-  }
-  return a;
+    return cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess ? p : nullptr;
+  }));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -47,6 +40,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+PFN_cuCtxGetCurrent_v4000 ctx_get_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
   });
   return fn;
 }
@@ -157,6 +164,21 @@ WorkspaceLayout workspace_layout(const AttnGeom& g) {
 }
 
 }  // namespace
+
+void* current_context() {
+  PFN_cuCtxGetCurrent_v4000 get = ctx_get_current_fn();
+  if (get == nullptr) return nullptr;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return nullptr;
+  if (ctx == nullptr) {
+    // nothing current yet on this thread: cudaSetDevice makes the device's primary
+    // context current (and creates it if needed)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return nullptr;
+  }
+  return ctx;
+}
 
 RowAddr plain_rows(const int64_t stride[3], int B, int S) {
   RowAddr a;
