@@ -47,7 +47,6 @@ METRIC = "causal MHA fwd+bwd TFLOP/s and % bf16 tensor peak; relayout GB/s vs HB
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "llama70b"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-PROFILE_NOTES = os.path.join(ROOT, "profiles")
 
 
 # ---------------------------------------------------------------- accounting
@@ -126,17 +125,23 @@ def source_digest(names) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_note: str, sources) -> int | None:
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
-    path = os.path.join(PROFILE_NOTES, kernel_note)
-    if not os.path.exists(path):
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture of the
+# LLaMA-70B-shaped workload) per sp_attn_bwd call, keyed by the digest of the kernel code
+# they were measured on: a changed kernel has no recorded traffic until it is captured again.
+RECORDED_BWD_TRAFFIC = {
+    "workload": "llama70b",
+    "sources": ["attn_bwd.cu", "ptx.cuh"],
+    "by_digest": {"7d2f0bdee98a21e3": 9045071360},
+}
+
+
+def recorded_traffic(workload_name: str) -> int | None:
+    """DRAM bytes per sp_attn_bwd call for this workload if its kernel code is unchanged
+    since the capture, else None."""
+    rec = RECORDED_BWD_TRAFFIC
+    if workload_name != rec["workload"]:
         return None
-    text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
-    if not m or not d or d.group(1) != source_digest(sources):
-        return None
-    return int(m.group(1))
+    return rec["by_digest"].get(source_digest(rec["sources"]))
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -247,14 +252,34 @@ def oracle_sample(w, heads: int, prefix: int):
     return flops, dt, orc.threads(), heads, prefix
 
 
-def cpu_baseline(w, heads=4, prefix=8192):
-    flops, dt, cores, heads, prefix = oracle_sample(w, heads, prefix)
-    line = {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"fp64 C oracle, causal fwd+bwd of {heads} heads over the first {prefix} "
-                      f"positions of {w.name} (d={w.d}); {flops / 1e9:.1f} GFLOP in {dt:.1f} s"}
-    # the same oracle on one core, on a smaller sample of the same problem
+def head_of(t: torch.Tensor, w, j: int):
+    """Head j of a shard-layout tensor [N][b][s/N][h][d] over the whole sequence of batch
+    row 0, as the oracle's [1][s][1][d] fp64 array (the shards in order are the sequence)."""
+    return t[:, 0, :, j, :].reshape(1, w.s, 1, w.d).double().cpu().numpy()
+
+
+def cpu_baseline(w, ins, head=0):
+    """The oracle on the host cores over one whole head of the timed workload (every query
+    row and every key; inputs copied from the device), extrapolated linearly in heads to
+    the full workload, plus the same oracle on one core over a shorter sequence."""
     import oracle
     orc = oracle.default()
+    q, k, v, do = (head_of(ins[n], w, head) for n in ("q", "k", "v", "dout"))
+    kl = None if ins["key_len"] is None else ins["key_len"][:1].tolist()
+    t0 = time.perf_counter()
+    orc.attn_fwd(q, k, v, w.causal, 0, kl)
+    orc.attn_bwd(q, k, v, do, w.causal, 0, kl)
+    dt = time.perf_counter() - t0
+    flops = step_flops(w) / (w.b * w.h)            # one head of one batch row
+    full_s = dt * w.b * w.h
+    line = {"value": flops / dt / 1e12, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
+            "sample": f"fp64 C oracle, fwd+bwd of head {head} of batch row 0 over all {w.s} "
+                      f"positions of {w.name} (d={w.d}), inputs copied from the device: "
+                      f"{flops / 1e9:.1f} GFLOP in {dt:.1f} s",
+            "full_workload_s": full_s,
+            "full_workload_s_kind": f"extrapolated linearly in heads ({w.b * w.h} heads), "
+                                    "not measured"}
+    # the same oracle on one core, on a shorter sequence of the same problem
     threads = orc.threads()
     orc.set_threads(1)
     try:
@@ -352,6 +377,70 @@ def merge_bytes_per_step(w, chunks: int) -> int:
     per_elem = 6 + 10 * (chunks - 2) + 12 if chunks > 1 else 8
     per_row = 8 + 12 * (chunks - 1)
     return elems * per_elem + rows * per_row
+
+
+# Workloads measured after the headline in the default run (name, timed steps): the other
+# configurations, so that each reports its step rate, roofline fraction and relayout rate.
+OTHER_WORKLOADS = [("ulysses131k", 3), ("llama7b", 20), ("padded", 20)]
+
+
+def measure_workload(w, steps, warmup, device, peaks):
+    """Time `steps` device-resident steps of workload w (after `warmup` untimed ones) with
+    CUDA events on the launching stream, and each library call inside them."""
+    from sequence_head_attention_seq_b300 import UlyssesAttention, sp_get_device_status
+    ins = workloads.make_inputs(w, device=device)
+    timer = EventTimer()
+    step = UlyssesAttention(w.N, w.b, w.s, w.h, w.d, w.causal, key_len=ins["key_len"],
+                            device=device, timer=timer)
+    for _ in range(warmup):
+        step.forward(ins["q"], ins["k"], ins["v"])
+        step.backward(ins["dout"])
+    torch.cuda.synchronize()
+    timer.enabled = True
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step.forward(ins["q"], ins["k"], ins["v"])
+        step.backward(ins["dout"])
+    b.record()
+    torch.cuda.synchronize()
+    timer.enabled = False
+    if sp_get_device_status() != 0:
+        raise RuntimeError(f"device status reported an error in workload {w.name}")
+    ms = a.elapsed_time(b) / steps
+    per_step = timer.per_step_ms(steps)
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    fwd_f = attn_fwd_flops(w)
+    tf = step_flops(w) / (ms * 1e-3) / 1e12
+    out = {"steps": steps, "warmup": warmup, "ms_per_step": ms, "tflops": tf,
+           "frac_of_burst": tf / burst,
+           "attn_fwd_tflops": fwd_f / (per_step["attn_fwd"] * 1e-3) / 1e12,
+           "attn_bwd_tflops": 2.5 * fwd_f / (per_step["attn_bwd"] * 1e-3) / 1e12,
+           "valid_tflops": 14.0 * w.d * valid_pairs(w, ins["key_len"]) / (ms * 1e-3) / 1e12,
+           "config": config_of(w)}
+    relayout_ms = sum(per_step.get(n, 0.0) for n in ("seq2head_qkv", "head2seq_o", "seq2head_do",
+                                                       "head2seq_grads"))
+    if relayout_ms > 0:
+        gbs = relayout_bytes_per_step(w) / (relayout_ms * 1e-3) / 1e9
+        out["relayout"] = {"gbs": gbs, "frac": gbs / hbm, "ms_per_step": relayout_ms}
+    return out
+
+
+def measure_other_workloads(warmup, device, peaks, local):
+    clocks = ClockSampler(gpu_index_for(local))
+    clocks.start()
+    res = {}
+    try:
+        for name, steps in OTHER_WORKLOADS:
+            res[name] = measure_workload(workloads.WORKLOADS[name], steps, warmup, device, peaks)
+            torch.cuda.empty_cache()
+    finally:
+        clocks.stop()
+    res["clocks"] = clocks.summary()
+    res["peaks"] = "burst bf16 and HBM copy from " + ("MEASURED_PEAKS.json" if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else "the fallback figures")
+    return res
 
 
 def run_ours(args, w):
@@ -519,7 +608,8 @@ def run_ours(args, w):
     peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     bwd_tf = 2.5 * fwd_f / (bwd_ms * 1e-3) / 1e12
-    traffic = None if ring else recorded_traffic("attn_bwd_llama70b.md", ["attn_bwd.cu", "ptx.cuh"])
+    plain = not (ring or args.heads is not None or args.key_mask or args.fused or args.layer)
+    traffic = recorded_traffic(w.name) if plain else None
     relayout_ms = sum(calls.get(n, 0.0) for n in ("seq2head_qkv", "head2seq_o", "seq2head_do",
                                                     "head2seq_grads"))
     relayout = None
@@ -582,9 +672,13 @@ def run_ours(args, w):
         "roofline": {"kernel": (f"sp_attn_bwd over {args.ring} key chunks (statistics + tcgen05 "
                                 "main + dQ convert each)") if ring else
                                "sp_attn_bwd (statistics + tcgen05 main + dQ convert)",
-                     "bound": "tensor", "achieved": bwd_tf, "peak": peak_sus, "unit": "TFLOP/s",
-                     "frac": bwd_tf / peak_sus, "peak_kind": f"{peak_kind} sustained bf16",
-                     "frac_of_burst": bwd_tf / peak_burst, "traffic": traffic,
+                     # the call lasts tens of milliseconds inside a step well under a
+                     # second: the burst peak is its denominator, the sustained one beside it
+                     "bound": "tensor", "achieved": bwd_tf, "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": bwd_tf / peak_burst,
+                     "peak_kind": f"{peak_kind} burst bf16",
+                     "frac_sustained": bwd_tf / peak_sus, "peak_sustained": peak_sus,
+                     "traffic": traffic,
                      "algorithmic_flops_per_launch": 2.5 * fwd_f},
         "relayout": relayout,
         "kernels": kernels,
@@ -595,7 +689,14 @@ def run_ours(args, w):
         "clocks": clock_summary,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, ins)
+    default_run = not (args.ring or args.layer or args.fused or args.key_mask or args.graph or
+                       args.heads is not None) and w.name == DEFAULT_WORKLOAD
+    if world == 1 and default_run and not args.no_workloads:
+        # free the headline's buffers before the other workloads allocate theirs
+        ins = step = host_step = host_in = host_out = None
+        torch.cuda.empty_cache()
+        line["workloads"] = measure_other_workloads(max(args.warmup, 3), device, peaks, local)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -611,6 +712,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads that the default run times after the headline")
     ap.add_argument("--ring", type=int, default=0,
                     help="run the attention blockwise over this many key chunks (ring attention "
                          "on one GPU: chunked forward + merge, chunked backward)")

@@ -23,7 +23,7 @@
  *        shards [b, s/N, h, d]; the all-to-all regroups them so that every
  *        rank holds the full sequence for a subset of heads.
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings taken where the pages are silent:
  *  - key padding is right padding: key j of batch b is valid iff
  *    j < key_len[b];
  *  - a general key mask (the transformers PR 31525 collator's
