@@ -640,9 +640,12 @@ def run_ours(args, w):
             entry["tflops"] = 2.5 * fwd_f / (per_step[n] * 1e-3) / 1e12
             entry["valid_tflops"] = 10.0 * w.d * pairs / (per_step[n] * 1e-3) / 1e12
         elif n.startswith("proj_"):
+            # the tcgen05 GEMMs of the projections (forward: one product; backward: the
+            # input and the weight gradient)
             M, dim, hd = w.b * w.s, w.h * w.d, w.h * w.d
             f = 2.0 * M * dim * (3 * hd if "qkv" in n else hd) * (2 if n.endswith("_bwd") else 1)
             entry["tflops"] = f / (ms * 1e-3) / 1e12
+            entry["frac_of_burst"] = entry["tflops"] / peak_burst
         elif n == "ring_merge":
             entry["ms_per_step"] = per_step[n]
             nbytes = merge_bytes_per_step(w, args.ring)

@@ -264,7 +264,8 @@ sp_status sp_attn_merge(const sp_merge_params* p, void* stream);
  *   sp_linear_bwd : dx[M][in] = dy[M][out] . W          (skipped when dx is NULL)
  *                   dW[out][in] = dy^T . x, or += with accumulate_dw = 1 (skipped when
  *                   dw is NULL)
- * bf16 in and out, fp32 accumulation; plain GEMMs on cuBLASLt without workspace.
+ * bf16 in and out, fp32 accumulation, on the library's own tcgen05 GEMM (128 x 256 tiles,
+ * TMA-fed, persistent); nothing is allocated.
  * All pointers DEVICE, 16-byte aligned.  Errors: M < 0, in or out < 1, accumulate_dw
  * not 0/1, required pointers NULL -> SP_ERR_INVALID_ARG; in or out not a multiple of 8,
  * misaligned pointers -> SP_ERR_MISALIGNED; a failed GEMM -> SP_ERR_CUDA.

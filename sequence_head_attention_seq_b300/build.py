@@ -25,7 +25,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsp.so")
 
 SOURCES = ["sp_abi.cu", "relayout.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_merge.cu",
-           "linear.cu", "attn_bwd_noalloc.cu", "host_step.cu"]
+           "linear.cu", "gemm.cu", "attn_bwd_noalloc.cu", "host_step.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -72,8 +72,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
     tmp = LIB + ".tmp%d" % os.getpid()
-    # cuBLASLt (the projection GEMMs) is the only shared-library dependency
-    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lcublasLt"]
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

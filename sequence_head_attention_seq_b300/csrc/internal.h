@@ -44,6 +44,10 @@ class ContextAddressCache {
   int n_ = 0;
 };
 
+// Device address of the status word that kernels OR error codes into, in the current
+// context (null if it cannot be found).
+uint32_t* status_word();
+
 constexpr int kMaxRelayoutTensors = SP_MAX_RELAYOUT_TENSORS;
 
 // shard_row: element pitch of a shard-side row (0: h*d; 3*h*d for packed Q/K/V, whose
@@ -126,6 +130,27 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int d, int heads_total,
 // 2-D TMA map over the fp32 dQ accumulator viewed as [rows_total][d], box = 32
 // columns x 32 rows, 128-byte swizzle (the backward reduces dQ tiles into it).
 bool encode_acc_map(CUtensorMap* map, const float* base, int d, int64_t rows_total);
+
+// 2-D TMA map over a bf16 matrix of `outer` rows of `inner` elements at a pitch of
+// `pitch` elements, box = box_inner x box_outer, 128-byte swizzle (box_inner = 64).
+bool encode_2d_bf16_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                        int64_t pitch, uint32_t box_inner, uint32_t box_outer);
+
+// C[M][N] (+)= sum_k A[m][k] B[n][k] in bf16 with fp32 accumulation (gemm.cu).  A is
+// K-major ([M][K], pitch lda) or, with a_mn, MN-major ([K][M]); B likewise ([N][K] or
+// [K][N], pitch ldb); C row-major with pitch ldc.  All pitches and N multiples of 8
+// elements, all pointers 16-byte aligned.
+struct GemmArgs {
+  const void* a;
+  const void* b;
+  void* c;
+  int64_t lda, ldb, ldc;
+  int M, N, K;
+  bool a_mn, b_mn;
+  bool accumulate;
+  uint32_t* status;
+};
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 
 struct FwdArgs {
   CUtensorMap tq, tk, tv;

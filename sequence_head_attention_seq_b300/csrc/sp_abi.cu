@@ -22,14 +22,6 @@ namespace {
 
 ContextAddressCache g_status_addr;
 
-// Device address of the status word in the current context (looked up once per context).
-uint32_t* status_word() {
-  return static_cast<uint32_t*>(g_status_addr.get([]() -> void* {
-    void* p = nullptr;
-    return cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess ? p : nullptr;
-  }));
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -178,6 +170,29 @@ void* current_context() {
     if (get(&ctx) != CUDA_SUCCESS) return nullptr;
   }
   return ctx;
+}
+
+// Device address of the status word in the current context (looked up once per context).
+uint32_t* status_word() {
+  return static_cast<uint32_t*>(g_status_addr.get([]() -> void* {
+    void* p = nullptr;
+    return cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess ? p : nullptr;
+  }));
+}
+
+bool encode_2d_bf16_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer,
+                        int64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr || inner < 1 || outer < 1) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t elem[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 RowAddr plain_rows(const int64_t stride[3], int B, int S) {

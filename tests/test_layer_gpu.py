@@ -41,6 +41,44 @@ def test_linear_matches_oracle(M, n_in, n_out):
     check_grad(f64(dw2), 2 * rdw, "dw accumulated twice")
 
 
+def _check_rounded(got: np.ndarray, ref: np.ndarray, what: str, roundings: int = 1):
+    """Element by element: the inputs are bf16 values (exact in fp64), so the only errors
+    are the fp32 accumulation order (far below bf16's precision) and the rounding of the
+    result to bf16 (at most 2^-9 relative, once per rounding)."""
+    bound = roundings * 2.0 ** -8 * np.abs(ref) + 1e-5 * max(np.abs(ref).max(), 1e-30)
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} elements off, worst at "
+                           f"{np.unravel_index(np.argmax(np.abs(got - ref) - bound), ref.shape)}")
+
+
+@pytest.mark.parametrize("M,n_in,n_out", [
+    (4100, 520, 776),      # every dimension ragged against the 128 x 256 x 64 tiles
+    (8192, 1024, 2048),    # several tiles per persistent CTA in all three products
+    (200, 24, 40),         # k shorter than one 64-wide stage
+    (129, 8, 8),           # the smallest row width
+])
+def test_linear_elementwise(M, n_in, n_out):
+    """The tcgen05 GEMM behind the projections, every output element against the fp64
+    oracle: y = x W^T (both operands k-contiguous), dx = dy W (W read n-contiguous) and
+    dW (+)= dy^T x (both operands read m/n-contiguous)."""
+    need_gpu()
+    x = _randn((M, n_in), 7 * M + 1)
+    w = _randn((n_out, n_in), 7 * M + 2, n_in ** -0.5)
+    dy = _randn((M, n_out), 7 * M + 3)
+    y = sp_linear_fwd(x, w)
+    dx, dw = sp_linear_bwd(dy, x, w)
+    dw2 = dw.clone()
+    sp_linear_bwd(dy, x, w, dx=None, dw=dw2, accumulate_dw=True, need_dx=False)
+    torch.cuda.synchronize()
+    check_status()
+    ry = oracle.linear_fwd(f64(x), f64(w))
+    rdx, rdw = oracle.linear_bwd(f64(dy), f64(x), f64(w))
+    _check_rounded(f64(y), ry, "y")
+    _check_rounded(f64(dx), rdx, "dx")
+    _check_rounded(f64(dw), rdw, "dw")
+    _check_rounded(f64(dw2), 2 * rdw, "dw accumulated twice", roundings=2)
+
+
 @pytest.mark.parametrize("N,b,s,h,d,dim", [(2, 1, 512, 4, 64, 256), (4, 2, 1024, 8, 128, 512)])
 def test_layer_matches_oracle(N, b, s, h, d, dim):
     need_gpu()
