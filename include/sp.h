@@ -11,7 +11,8 @@
  *  - Argument errors are detected on the host and returned BEFORE anything is
  *    launched (SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_MISALIGNED).
  *  - A failed launch returns SP_ERR_CUDA.  Faults found while the kernels run
- *    (a device wait that gave up) are reported by sp_get_device_status().
+ *    (a device wait that gave up, a key length outside [0, sk] read from device
+ *    memory) are reported by sp_get_device_status().
  *  - Calls are thread-safe; the library holds no per-call state.
  */
 #ifndef SP_H
@@ -148,7 +149,9 @@ typedef struct sp_attn_params {
     int causal;               /* 0 or 1 */
     int q_offset;             /* global sequence position of query row 0 (>= 0) */
     int kv_offset;            /* global sequence position of key row 0 (>= 0) */
-    const int32_t* key_len;   /* NULL, or DEVICE [B] valid-key counts in [0, sk] */
+    const int32_t* key_len;   /* NULL, or DEVICE [B] valid-key counts in [0, sk]; a count
+                                 outside that range is clamped into it and reported by
+                                 sp_get_device_status as SP_ERR_INVALID_ARG */
     float softmax_scale;      /* <= 0 selects 1/sqrt(d) */
     int dq_accumulate;        /* sp_attn_bwd only, 0 or 1: see sp_attn_bwd */
     const uint8_t* key_mask;  /* NULL, or DEVICE bytes [B][key_mask_stride]: key j of batch
@@ -382,9 +385,11 @@ sp_status sp_selftest_wait_timeout(void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word that the
- * kernels set when a bounded device-side wait gives up (SP_ERR_TIMEOUT) or a
- * launch-time invariant fails inside a kernel.  SP_ERR_CUDA if the stream
- * reports an error.
+ * kernels set since the last read: SP_ERR_TIMEOUT when a bounded device-side wait
+ * gave up; SP_ERR_INVALID_ARG when the only event was a key_len entry outside
+ * [0, sk] (the kernels clamped it, so their results are those of the clamped
+ * length); SP_ERR_CUDA for a failed launch-time invariant inside a kernel or a
+ * stream that reports an error.
  */
 sp_status sp_get_device_status(void* stream);
 

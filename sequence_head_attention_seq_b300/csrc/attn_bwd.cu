@@ -196,9 +196,16 @@ struct BwdKernelParams {
   uint32_t* status;
 };
 
-__device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
+// Valid keys of batch entry b: key_len[b] clamped into [0, sk].  A length outside that
+// range is also reported in the status word (once per CTA), so that the host learns of
+// it from sp_get_device_status while the results stay those of the clamped length.
+__device__ __forceinline__ int kv_limit(const AttnGeom& g, int b, uint32_t* status) {
   int n = g.sk;
-  if (g.key_len != nullptr) n = min(n, max(__ldg(g.key_len + b), 0));
+  if (g.key_len != nullptr) {
+    const int kl = __ldg(g.key_len + b);
+    if ((kl < 0 || kl > g.sk) && threadIdx.x == 0) raise_status(status, kStatusBadKeyLen);
+    n = min(n, max(kl, 0));
+  }
   return n;
 }
 
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
   }
   const int b = bh / g.H, h = bh % g.H;
   const int kv0 = n * kKeys;
-  const int kvlen = kv_limit(g, b);
+  const int kvlen = kv_limit(g, b, p.status);
   const int m_start = g.causal ? max(0, kv0 - g.q_offset) / kRows : 0;
   const int m_end = (g.sq + kRows - 1) / kRows;
   // key mask: does the block hold a masked key below kvlen, and a visible one at all?

@@ -67,9 +67,16 @@ struct TileInfo {
   int nblocks;   // KV blocks it needs
 };
 
-__device__ __forceinline__ int kv_limit(const AttnGeom& g, int b) {
+// Valid keys of batch entry b: key_len[b] clamped into [0, sk].  A length outside that
+// range is also reported in the status word (once per CTA), so that the host learns of
+// it from sp_get_device_status while the results stay those of the clamped length.
+__device__ __forceinline__ int kv_limit(const AttnGeom& g, int b, uint32_t* status) {
   int n = g.sk;
-  if (g.key_len != nullptr) n = min(n, max(__ldg(g.key_len + b), 0));
+  if (g.key_len != nullptr) {
+    const int kl = __ldg(g.key_len + b);
+    if ((kl < 0 || kl > g.sk) && threadIdx.x == 0) raise_status(status, kStatusBadKeyLen);
+    n = min(n, max(kl, 0));
+  }
   return n;
 }
 
@@ -108,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   cta_order(blockIdx.x, p.num_pairs, p.group_shift, &bh, &cls);
   const int pair = p.num_pairs - 1 - cls;   // causal: the last query tiles carry most work
   const int b = bh / g.H, h = bh % g.H;
-  const int kvlen = kv_limit(g, b);
+  const int kvlen = kv_limit(g, b, p.status);
   const TileInfo ti[2] = {tile_info(g, kvlen, pair * 2 * kRows),
                           tile_info(g, kvlen, pair * 2 * kRows + kRows)};
   const int nmax = max(ti[0].nblocks, ti[1].nblocks);

@@ -20,6 +20,7 @@ enum : uint32_t {
   kStatusTimeout = 1u << 0,   // an mbarrier wait exceeded its limit
   kStatusBadSmem = 1u << 1,   // dynamic shared memory not 1024-byte aligned
   kStatusBadTmem = 1u << 2,   // TMEM allocation returned an unexpected base
+  kStatusBadKeyLen = 1u << 3, // a key length outside [0, sk] (clamped into it)
 };
 
 #ifndef SP_WAIT_LIMIT_NS

@@ -521,6 +521,7 @@ sp_status sp_get_device_status(void* stream) {
   if (cudaMemsetAsync(addr, 0, sizeof word, s) != cudaSuccess) return SP_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SP_ERR_CUDA;
   if (word & kStatusTimeout) return SP_ERR_TIMEOUT;
+  if (word == kStatusBadKeyLen) return SP_ERR_INVALID_ARG;
   if (word != 0) return SP_ERR_CUDA;
   return SP_OK;
 }

@@ -20,12 +20,13 @@ def _randn(shape, seed, scale=1.0):
     return workloads.randn_bf16(shape, seed, scale, device="cuda")
 
 
-def _run(q, k, v, do, causal, q_offset=0, key_len=None):
+def _run(q, k, v, do, causal, q_offset=0, key_len=None, check=True):
     kl = None if key_len is None else torch.tensor(key_len, dtype=torch.int32, device="cuda")
     o, lse = sp_attn_fwd(q, k, v, causal, q_offset, kl)
     dq, dk, dv = sp_attn_bwd(q, k, v, o, lse, do, causal, q_offset, kl)
     torch.cuda.synchronize()
-    check_status()
+    if check:
+        check_status()
     return o, lse, dq, dk, dv
 
 
@@ -145,13 +146,17 @@ def test_empty_rows():
     assert not dq[0].any() and not dk[0].any() and not dv[0].any()
 
 
-def test_out_of_range_key_len_is_clamped():
+def test_out_of_range_key_len_is_clamped_and_reported():
     """A length below 0 hides every key and one above sk hides none: the results are
-    those of [0, sk], bit for bit (dq within the gradient bar)."""
+    those of [0, sk], bit for bit (dq within the gradient bar), and the device status
+    reports the bad lengths once (SP_ERR_INVALID_ARG), then reads clean again."""
     need_gpu()
+    from sequence_head_attention_seq_b300 import sp_get_device_status
     q, do = _randn((2, 130, 1, 64), 96), _randn((2, 130, 1, 64), 97)
     k, v = _randn((2, 140, 1, 64), 98), _randn((2, 140, 1, 64), 99)
-    a = _run(q, k, v, do, False, key_len=[-3, 190])
+    a = _run(q, k, v, do, False, key_len=[-3, 190], check=False)
+    assert sp_get_device_status() == 1, "SP_ERR_INVALID_ARG expected for lengths outside [0, sk]"
+    assert sp_get_device_status() == 0
     b = _run(q, k, v, do, False, key_len=[0, 140])
     for name, x, y in zip(("o", "lse", "dk", "dv"), (a[0], a[1], a[3], a[4]),
                           (b[0], b[1], b[3], b[4])):
