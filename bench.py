@@ -386,6 +386,46 @@ def merge_bytes_per_step(w, chunks: int) -> int:
 OTHER_WORKLOADS = [("ulysses131k", 3), ("llama7b", 20), ("padded", 20)]
 
 
+def host_link(host_in, host_out, device, reps: int = 2):
+    """Copy rates between the step's page-locked host buffers and the device: each
+    direction alone and both at once (the end-to-end step moves both directions while
+    its kernels run), timed with CUDA events around plain whole-tensor copies."""
+    dev_in = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in host_in]
+    dev_out = [torch.empty(t.shape, dtype=t.dtype, device=device) for t in host_out]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    legs = {"h2d": (s_in, list(zip(dev_in, host_in))), "d2h": (s_out, list(zip(host_out, dev_out)))}
+
+    def run(which):
+        cur = torch.cuda.current_stream(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        ends = []
+        for name in which:
+            st, pairs = legs[name]
+            st.wait_event(e0)
+            with torch.cuda.stream(st):
+                for _ in range(reps):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(st)
+            ends.append(ev)
+        for ev in ends:
+            cur.wait_event(ev)
+        e1.record(cur)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps
+
+    run(("h2d", "d2h"))   # warm-up
+    nbytes = sum(t.numel() * t.element_size() for t in host_in)
+    ms = {k: run(v) for k, v in (("h2d", ("h2d",)), ("d2h", ("d2h",)),
+                                 ("both", ("h2d", "d2h")))}
+    return {"h2d_gbs": nbytes / (ms["h2d"] * 1e-3) / 1e9,
+            "d2h_gbs": nbytes / (ms["d2h"] * 1e-3) / 1e9,
+            "both_gbs_each_way": nbytes / (ms["both"] * 1e-3) / 1e9,
+            "both_ms": ms["both"], "bytes_each_way": nbytes}
+
+
 def measure_workload(w, steps, warmup, device, peaks):
     """Time `steps` device-resident steps of workload w (after `warmup` untimed ones) with
     CUDA events on the launching stream, and each library call inside them."""
@@ -594,6 +634,13 @@ def run_ours(args, w):
         e2e = {"value": world * step_flops(w) / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": 4 * tensor_bytes(w), "d2h_bytes_per_step": 4 * tensor_bytes(w),
                "ms_per_step": e2e_ms, "api": e2e_api}
+        # the end-to-end step can take no less than the longer of the device step and
+        # the time the host link needs to move its inputs in and its results out at once
+        link = host_link(list(host_in.values()), host_out, device)
+        bound = max(link["both_ms"], ms_per_step)
+        e2e["link"] = {**link, "bound_ms": bound, "frac_of_bound": bound / e2e_ms,
+                       "bound_basis": "max(device step, both directions' copies measured at "
+                                      "once on these buffers)"}
 
     clock_summary = clocks.summary()
     if rank != 0:
