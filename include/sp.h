@@ -5,7 +5,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Tensors are bf16 in DEVICE memory, owned by the caller; the library never
- *    allocates, frees or keeps a pointer after a call returns.
+ *    allocates, frees or keeps a pointer after a call returns.  Each buffer must hold
+ *    every element that its shape and strides address: the library cannot see
+ *    allocation sizes and does not check them.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call only
  *    enqueues work on it: no host synchronisation, no allocation.
  *  - Argument errors are detected on the host and returned BEFORE anything is
