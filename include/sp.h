@@ -175,9 +175,12 @@ typedef struct sp_attn_params {
  *
  * o   : DEVICE bf16, layout of q with o_stride.
  * lse : DEVICE fp32 [B][H][sq], contiguous.  Needed by sp_attn_bwd.
- * Errors: B, H, sq, sk < 0, q_offset < 0, kv_offset < 0, causal not 0/1, NULL
- *         pointers -> SP_ERR_INVALID_ARG (B, H, sq or sk equal to 0 is allowed:
- *         nothing to do, SP_OK); key_mask_stride < sk with a key_mask ->
+ * Empty sizes: B, H or sq equal to 0 leaves nothing to do (SP_OK, nothing launched);
+ *         sk = 0 leaves every row without a visible key (o = 0, lse = -inf).  A tensor
+ *         without elements may be NULL: q, o and lse when sq = 0, k and v when sk = 0,
+ *         all of them when B or H is 0.
+ * Errors: B, H, sq, sk < 0, q_offset < 0, kv_offset < 0, causal not 0/1, any other
+ *         NULL pointer -> SP_ERR_INVALID_ARG; key_mask_stride < sk with a key_mask ->
  *         SP_ERR_INVALID_ARG; d not 64/128, q_offset + sq or kv_offset + sk above
  *         2^30 -> SP_ERR_UNSUPPORTED; pointer/stride alignment (key_mask and its
  *         stride included) -> SP_ERR_MISALIGNED.
@@ -210,6 +213,8 @@ size_t sp_attn_bwd_workspace_size(const sp_attn_params* p);
  *              must be the previous call's.  The first chunk's call uses
  *              dq_accumulate = 0.  dk and dv are always this call's (this chunk's)
  *              gradients.
+ * Empty sizes as sp_attn_fwd: with sk = 0, dq = 0 (dk, dv have no elements and may be
+ * NULL); with sq = 0 and sk > 0, dk = dv = 0 (o, lse, dout and dq may be NULL).
  * Errors as sp_attn_fwd, plus SP_ERR_WORKSPACE when workspace_bytes is too small.
  */
 sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse,

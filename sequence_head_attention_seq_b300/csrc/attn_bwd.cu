@@ -777,7 +777,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     // heads start first (measured on B300: 32 heads x 4096 tokens 0.52 -> 0.49 ms;
     // 8 heads x 32768 tokens, where a group would overflow L2, keeps one head at a time).
     {
-      const int64_t per_head = rows * g.d * (2 + 2 + 4);
+      const int64_t per_head = std::max<int64_t>(1, rows * g.d * (2 + 2 + 4));   // 0 rows: sq = 0
       const int64_t l2 = device_l2_bytes();
       const int64_t cap = l2 > 0 ? std::min<int64_t>(8, (l2 / 2) / per_head) : 1;
       p.group_shift = group_shift(bh, cap);

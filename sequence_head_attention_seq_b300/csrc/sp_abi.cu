@@ -100,7 +100,12 @@ sp_status check_attn(const sp_attn_params* p, AttnGeom* g) {
   if (static_cast<int64_t>(p->q_offset) + p->sq > (int64_t(1) << 30) ||
       static_cast<int64_t>(p->kv_offset) + p->sk > (int64_t(1) << 30))
     return SP_ERR_UNSUPPORTED;
-  if (p->q == nullptr || p->k == nullptr || p->v == nullptr) return SP_ERR_INVALID_ARG;
+  // A tensor without elements may be a null pointer (PyTorch allocates none for it): q
+  // when there are no query rows, k and v when there are no keys.
+  const bool none = p->B == 0 || p->H == 0;
+  if ((p->q == nullptr && !(none || p->sq == 0)) ||
+      ((p->k == nullptr || p->v == nullptr) && !(none || p->sk == 0)))
+    return SP_ERR_INVALID_ARG;
   if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v)) return SP_ERR_MISALIGNED;
   if (!strides_ok(p->q_stride) || !strides_ok(p->k_stride) || !strides_ok(p->v_stride) ||
       !strides_ok(p->o_stride))
@@ -394,14 +399,15 @@ sp_status sp_attn_fwd(const sp_attn_params* p, void* o, float* lse, void* stream
   AttnGeom g;
   sp_status st = check_attn(p, &g);
   if (st != SP_OK) return st;
-  if (o == nullptr || lse == nullptr) return SP_ERR_INVALID_ARG;
   if (!aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return SP_ERR_MISALIGNED;
-  if (empty_problem(g)) return SP_OK;
-  FwdArgs a;
+  if (empty_problem(g)) return SP_OK;   // o and lse have no elements (may be null)
+  if (o == nullptr || lse == nullptr) return SP_ERR_INVALID_ARG;
+  FwdArgs a{};
   const Layouts L = layouts_of(p, g);
-  if (!encode_rows_map(&a.tq, p->q, g.d, L.heads_total, L.shards, L.q) ||
-      !encode_rows_map(&a.tk, p->k, g.d, L.heads_total, L.shards, L.k) ||
-      !encode_rows_map(&a.tv, p->v, g.d, L.heads_total, L.shards, L.v))
+  if (!encode_rows_map(&a.tq, p->q, g.d, L.heads_total, L.shards, L.q)) return SP_ERR_CUDA;
+  // no keys: every row gets out = 0 and lse = -inf, and no K or V tile is ever loaded
+  if (g.sk > 0 && (!encode_rows_map(&a.tk, p->k, g.d, L.heads_total, L.shards, L.k) ||
+                   !encode_rows_map(&a.tv, p->v, g.d, L.heads_total, L.shards, L.v)))
     return SP_ERR_CUDA;
   a.aq = L.q;
   a.ak = L.k;
@@ -426,8 +432,12 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
   AttnGeom g;
   sp_status st = check_attn(p, &g);
   if (st != SP_OK) return st;
-  if (o == nullptr || lse == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||
-      dv == nullptr)
+  // as for q, k, v: the tensors of the query rows may be null when there are none, dk
+  // and dv when there are no keys
+  const bool none = g.B == 0 || g.H == 0;
+  if (((o == nullptr || lse == nullptr || dout == nullptr || dq == nullptr) &&
+       !(none || g.sq == 0)) ||
+      ((dk == nullptr || dv == nullptr) && !(none || g.sk == 0)))
     return SP_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
@@ -438,7 +448,7 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
   if (static_cast<int64_t>(g.B) * g.H * padded_rows(g.sq) > INT32_MAX) return SP_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < w.total) return SP_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return SP_ERR_MISALIGNED;
-  BwdArgs a;
+  BwdArgs a{};
   const Layouts L = layouts_of(p, g);
   if (g.sq > 0 && g.sk > 0) {
     if (!encode_rows_map(&a.tq, p->q, g.d, L.heads_total, L.shards, L.q) ||

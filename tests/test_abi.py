@@ -107,6 +107,8 @@ def _params(**kw):
     (dict(sq=-1), INVALID),
     (dict(B=-2), INVALID),
     (dict(q=None), INVALID),
+    (dict(k=None), INVALID),                          # keys exist: k and v are required
+    (dict(v=None), INVALID),
     (dict(k=FAKE_ODD), MISALIGNED),
     (dict(q_stride=(ctypes.c_int64 * 3)(4, 4, 4)), MISALIGNED),
     (dict(key_len=FAKE + 2), MISALIGNED),
@@ -117,6 +119,22 @@ def test_attn_validation(lib, kw, code):
     assert lib.sp_attn_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                            1 << 40, None) == code
     assert lib.sp_attn_bwd_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_null_pointers_for_tensors_without_elements(lib):
+    """A tensor with no elements may be NULL (PyTorch gives empty tensors no storage):
+    here the problems are empty, so the calls return before anything is launched."""
+    p = _params(sq=0, q=None)
+    assert lib.sp_attn_fwd(ctypes.byref(p), None, None, None) == OK
+    p = _params(B=0, q=None, k=None, v=None)
+    assert lib.sp_attn_fwd(ctypes.byref(p), None, None, None) == OK
+    assert lib.sp_attn_bwd(ctypes.byref(p), None, None, None, None, None, None, FAKE, 1 << 20,
+                           None) == OK
+    # a problem with query rows still needs its outputs
+    p = _params(sk=0, k=None, v=None)
+    assert lib.sp_attn_fwd(ctypes.byref(p), None, FAKE, None) == INVALID
+    assert lib.sp_attn_bwd(ctypes.byref(p), FAKE, FAKE, FAKE, None, None, None, FAKE, 1 << 40,
+                           None) == INVALID
 
 
 def test_attn_output_pointer_validation(lib):

@@ -63,6 +63,32 @@ def test_small_against_oracle(case):
     check_grad(f64(dv), rdv, "dv")
 
 
+def test_no_keys_and_no_query_rows():
+    """Closed forms of the empty key and query sets: with sk = 0 no row sees a key (out
+    = 0, lse = -inf, dq = 0); with sq = 0 no key is seen by any row (dk = dv = 0, over
+    freshly allocated, uninitialised outputs).  The zero-element tensors reach the
+    library as null pointers."""
+    need_gpu()
+    B, H, d = 2, 3, 128
+    q = _randn((B, 70, H, d), 5)
+    do = _randn((B, 70, H, d), 6)
+    k = torch.empty((B, 0, H, d), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    for causal in (False, True):
+        o, lse, dq, dk, dv = _run(q, k, v, do, causal)
+        assert torch.count_nonzero(o) == 0
+        assert bool(torch.isneginf(lse).all())
+        assert torch.count_nonzero(dq) == 0
+        assert dk.shape == k.shape and dv.shape == v.shape
+    q0 = torch.empty((B, 0, H, d), dtype=torch.bfloat16, device="cuda")
+    k = _randn((B, 200, H, d), 7)
+    v = _randn((B, 200, H, d), 8)
+    for causal in (False, True):
+        o, lse, dq, dk, dv = _run(q0, k, v, torch.empty_like(q0), causal)
+        assert o.numel() == 0 and lse.numel() == 0 and dq.numel() == 0
+        assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
 def test_causal_row0_returns_v0_bit_exact():
     need_gpu()
     q, k, v = (_randn((2, 300, 4, 128), 40 + t) for t in range(3))
