@@ -245,6 +245,7 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse,
  *              rounded to bf16 (nearest even), for the last chunk
  * init != 0 starts a new accumulation: o_acc and lse_acc are overwritten with the
  * partial (their contents on entry are not read).
+ * B, H or sq equal to 0: nothing to merge (SP_OK; the tensors, all empty, may be NULL).
  * Errors: sizes < 0, d not 64/128 -> SP_ERR_INVALID_ARG / SP_ERR_UNSUPPORTED; NULL
  * required pointers -> SP_ERR_INVALID_ARG; pointers not 16-byte aligned or strides
  * not multiples of 8 -> SP_ERR_MISALIGNED.
@@ -276,6 +277,8 @@ sp_status sp_attn_merge(const sp_merge_params* p, void* stream);
  *                   dw is NULL)
  * bf16 in and out, fp32 accumulation, on the library's own tcgen05 GEMM (128 x 256 tiles,
  * TMA-fed, persistent); nothing is allocated.
+ * M = 0: x, y, dy and dx have no elements (nothing is written, and they may be NULL);
+ * dy^T . x is then the zero matrix, so dW is cleared (kept with accumulate_dw = 1).
  * All pointers DEVICE, 16-byte aligned.  Errors: M < 0, in or out < 1, accumulate_dw
  * not 0/1, required pointers NULL -> SP_ERR_INVALID_ARG; in or out not a multiple of 8,
  * misaligned pointers -> SP_ERR_MISALIGNED; a failed GEMM -> SP_ERR_CUDA.

@@ -33,7 +33,8 @@ sp_status sp_linear_fwd(const void* x, const void* w, void* y, int M, int in, in
                         void* stream) {
   const sp_status st = check_linear(M, in, out);
   if (st != SP_OK) return st;
-  if (x == nullptr || w == nullptr || y == nullptr) return SP_ERR_INVALID_ARG;
+  // x and y have no elements when M = 0 and may then be null
+  if (w == nullptr || (M > 0 && (x == nullptr || y == nullptr))) return SP_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return SP_ERR_MISALIGNED;
   if (M == 0) return SP_OK;
   GemmArgs g{x, w, y, in, in, out, M, out, in, false, false, false, status_word()};
@@ -44,14 +45,23 @@ sp_status sp_linear_bwd(const void* dy, const void* x, const void* w, void* dx, 
                         int in, int out, int accumulate_dw, void* stream) {
   const sp_status st = check_linear(M, in, out);
   if (st != SP_OK) return st;
-  if (dy == nullptr || x == nullptr || w == nullptr || (dx == nullptr && dw == nullptr))
+  // dy and x have no elements when M = 0 and may then be null
+  if (w == nullptr || (M > 0 && (dy == nullptr || x == nullptr)) ||
+      (dx == nullptr && dw == nullptr))
     return SP_ERR_INVALID_ARG;
   if (accumulate_dw != 0 && accumulate_dw != 1) return SP_ERR_INVALID_ARG;
   if (!aligned16(dy) || !aligned16(x) || !aligned16(w) || (dx && !aligned16(dx)) ||
       (dw && !aligned16(dw)))
     return SP_ERR_MISALIGNED;
-  if (M == 0) return SP_OK;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    // no rows: dx has no elements and dy^T . x is the zero matrix, so a dW that is not
+    // accumulated into is cleared (one accumulated into keeps its value)
+    if (dw != nullptr && accumulate_dw == 0 &&
+        cudaMemsetAsync(dw, 0, static_cast<size_t>(out) * in * 2, s) != cudaSuccess)
+      return SP_ERR_CUDA;
+    return SP_OK;
+  }
   uint32_t* status = status_word();
   // dx[M][in] = dy[M][out] . W[out][in]: k = out; W read with n = in contiguous
   if (dx != nullptr) {

@@ -484,8 +484,10 @@ sp_status sp_attn_merge(const sp_merge_params* p, void* stream) {
   if (p == nullptr) return SP_ERR_INVALID_ARG;
   if (p->B < 0 || p->H < 0 || p->sq < 0) return SP_ERR_INVALID_ARG;
   if (p->d != 64 && p->d != 128) return SP_ERR_UNSUPPORTED;
-  if (p->o_part == nullptr || p->lse_part == nullptr || p->o_acc == nullptr ||
-      p->lse_acc == nullptr)
+  // with no rows every tensor is empty and may be null
+  const bool none = p->B == 0 || p->H == 0 || p->sq == 0;
+  if (!none && (p->o_part == nullptr || p->lse_part == nullptr || p->o_acc == nullptr ||
+                p->lse_acc == nullptr))
     return SP_ERR_INVALID_ARG;
   if (!aligned16(p->o_part) || !aligned16(p->o_acc) || !strides_ok(p->part_stride) ||
       (reinterpret_cast<uintptr_t>(p->lse_part) & 3u) != 0 ||

@@ -187,6 +187,7 @@ def _merge(**kw):
     (dict(part_stride=(ctypes.c_int64 * 3)(4, 4, 4)), MISALIGNED),
     (dict(o_out=FAKE_ODD), MISALIGNED),
     (dict(B=0), OK),                                  # nothing to merge, nothing launched
+    (dict(sq=0, o_part=None, lse_part=None, o_acc=None, lse_acc=None), OK),   # empty: NULL ok
 ])
 def test_merge_validation(lib, kw, code):
     p = _merge(**kw)
@@ -225,6 +226,11 @@ def test_linear_validation(lib):
     assert f(None, FAKE, FAKE, 4, 64, 64, None) == INVALID
     assert f(FAKE_ODD, FAKE, FAKE, 4, 64, 64, None) == MISALIGNED
     assert f(FAKE, FAKE, FAKE, 0, 64, 64, None) == OK                  # no rows: nothing
+    assert f(None, FAKE, None, 0, 64, 64, None) == OK                  # ... x, y may be NULL
+    assert f(FAKE, None, FAKE, 0, 64, 64, None) == INVALID             # W is still required
+    # no rows, dW accumulated into: unchanged, nothing launched; dy, x, dx may be NULL
+    assert g(None, None, FAKE, None, FAKE, 0, 64, 64, 1, None) == OK
+    assert g(None, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 0, None) == INVALID   # rows need dy
     assert g(FAKE, FAKE, FAKE, None, None, 4, 64, 64, 0, None) == INVALID   # nothing to do
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 64, 2, None) == INVALID
     assert g(FAKE, FAKE, FAKE, FAKE_ODD, FAKE, 4, 64, 64, 0, None) == MISALIGNED

@@ -79,6 +79,23 @@ def test_linear_elementwise(M, n_in, n_out):
     _check_rounded(f64(dw2), 2 * rdw, "dw accumulated twice", roundings=2)
 
 
+def test_linear_zero_rows():
+    """M = 0: y and dx have no elements, dW = dy^T x is the zero matrix (cleared over an
+    uninitialised buffer), and a dW accumulated into keeps its value."""
+    need_gpu()
+    w = _randn((40, 72), 5)
+    x = torch.empty((0, 72), dtype=torch.bfloat16, device="cuda")
+    dy = torch.empty((0, 40), dtype=torch.bfloat16, device="cuda")
+    assert sp_linear_fwd(x, w).shape == (0, 40)
+    dw = torch.full_like(w, 3.0)
+    dx, dw = sp_linear_bwd(dy, x, w, dw=dw)
+    kept = sp_linear_bwd(dy, x, w, dw=torch.full_like(w, 3.0), accumulate_dw=True)[1]
+    torch.cuda.synchronize()
+    check_status()
+    assert dx.shape == (0, 72) and torch.count_nonzero(dw) == 0
+    assert bool((kept == 3.0).all())
+
+
 @pytest.mark.parametrize("N,b,s,h,d,dim", [(2, 1, 512, 4, 64, 256), (4, 2, 1024, 8, 128, 512)])
 def test_layer_matches_oracle(N, b, s, h, d, dim):
     need_gpu()
