@@ -56,6 +56,7 @@ def _check_rounded(got: np.ndarray, ref: np.ndarray, what: str, roundings: int =
     (8192, 1024, 2048),    # several tiles per persistent CTA in all three products
     (200, 24, 40),         # k shorter than one 64-wide stage
     (129, 8, 8),           # the smallest row width
+    (1, 72, 264),          # one row: dW contracts over a single row, one ragged tile each
 ])
 def test_linear_elementwise(M, n_in, n_out):
     """The tcgen05 GEMM behind the projections, every output element against the fp64
