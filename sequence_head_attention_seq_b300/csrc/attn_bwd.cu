@@ -25,8 +25,9 @@
 //      dQ_i is read out of TMEM at once by a drain warpgroup (so the next tile's dP^T
 //      can reuse the columns) and added into the fp32 workspace: for d = 128 straight
 //      from registers (TMEM lanes are head-dim indices, so a warp's 32 lanes add one
-//      contiguous 128-byte piece of a dQ row); for d = 64 staged in the dS tile and
-//      added by TMA tensor reduce-adds.
+//      contiguous 128-byte piece of a dQ row); for d = 64 by 16-byte vector reductions
+//      into an accumulator laid out [16][rows][4] per head (TMEM lanes are queries, so
+//      a warp's 32 lanes add 512 contiguous bytes).
 //   3. bwd_dq_convert: dq = bf16(scale * accumulator).  Bandwidth bound.
 #include <algorithm>
 #include <type_traits>
@@ -49,7 +50,9 @@ constexpr int kThreads = 512;
 constexpr uint32_t kRegsControl = 72, kRegsCompute = 152, kRegsDrain = 136;
 static_assert(kRegsControl + 2 * kRegsCompute + kRegsDrain == 4 * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr unsigned kDrainPaceNs = 30;   // sleep between pairs of dQ reductions (d = 128)
+// Sleep between pairs of 128-byte dQ reductions (d = 128), and twice that between
+// 512-byte ones (d = 64): the same rate of bytes per drain warp.
+constexpr unsigned kDrainPaceNs = 30;
 
 // ---------------------------------------------------------------- 1. row statistics
 
@@ -160,6 +163,30 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   *reinterpret_cast<uint4*>(dq + aq.off(b, static_cast<int>(i), h) + c * 8) = out;
 }
 
+// d = 64: the accumulator holds each head as [16][rows][4] (four consecutive head-dim
+// entries of a row side by side).  Thread = one row: 16 loads of 16 bytes, adjacent
+// threads on adjacent rows.
+__global__ void __launch_bounds__(256) bwd_dq_convert_d4_kernel(const float* __restrict__ dq_acc,
+                                                                __nv_bfloat16* __restrict__ dq,
+                                                                const RowAddr aq, int B, int H,
+                                                                int sq, int64_t rows, float scale) {
+  constexpr int D = 64;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<int64_t>(B) * H * sq) return;
+  const int64_t i = t % sq;
+  const int64_t bh = t / sq;
+  const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + bh * rows * D) + i;
+  __nv_bfloat16* out = dq + aq.off(b, static_cast<int>(i), h);
+#pragma unroll
+  for (int g = 0; g < D / 8; ++g) {
+    const float4 x = src[(2 * g) * rows], y = src[(2 * g + 1) * rows];
+    *reinterpret_cast<uint4*>(out + g * 8) =
+        make_uint4(pack_bf16x2(x.x * scale, x.y * scale), pack_bf16x2(x.z * scale, x.w * scale),
+                   pack_bf16x2(y.x * scale, y.y * scale), pack_bf16x2(y.z * scale, y.w * scale));
+  }
+}
+
 // ---------------------------------------------------------------- 2. main kernel
 
 template <int D>
@@ -177,16 +204,15 @@ struct BwdSmem {
   // next dO load then starts half a tile earlier than the Q load of the same stage
   uint64_t kv_full, q_full[2], do_full[2], q_empty[2], do_empty[2], s_full, dp_full, p_full[2],
       pds[2],
-      ds_empty, stage_free, dq_full, dq_empty, dkv_full, drain;
+      ds_empty, dq_full, dq_empty, dkv_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct BwdKernelParams {
   CUtensorMap tq, tk, tv, tdo;
-  CUtensorMap tdq;        // fp32 dQ accumulator as [B*H*rows][D], 32 x 32 boxes
   const float* stats;     // [B][H][2][rows]: -lse*log2(e), D
-  float* dq_acc;          // [B][H][rows][D]
+  float* dq_acc;          // [B][H] blocks of rows * D: [rows][D] (d = 128), [D/4][rows][4] (d = 64)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   RowAddr aq, ak, av;     // row layouts of q and dO (TMA), k/dk, v/dv
@@ -222,7 +248,7 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b, uint32_t* stat
 //   [0,128)   S^T (query half h in [64h, 64h+64)); each warpgroup writes its P^T (bf16)
 //             over the first 32 columns of the S^T half it has read
 //   [128,256) dP^T; once both halves are read, dQ^T (d = 128: lanes = head-dim
-//             indices, columns = queries) or dQ (d = 64: lanes = queries)
+//             indices, columns = queries) or dQ (d = 64: lanes = queries, columns = d)
 //   [256,256+D) dK accumulator, [256+D,256+2D) dV accumulator
 // Per query tile i the MMA thread issues
 //   (dQ_{i-1} read out) dP^T_i | (P^T_i half h in TMEM) dV += P^T_h dO_h, h = 0, 1 |
@@ -240,11 +266,12 @@ __device__ __forceinline__ int kv_limit(const AttnGeom& g, int b, uint32_t* stat
 // of one thread run in issue order), and the warpgroups write the next dS only after
 // the dK and dQ products of this tile have finished reading the dS tile.
 //
-// d = 64: dQ leaves through shared memory.  After the dK and dQ products complete, the
-// dS tile has no reader left, so each drain warp stages its 32 query rows as two
-// 32 x 32 boxes in two 4 KB slices of that tile and one lane issues TMA reduce-adds of
-// them into the accumulator; once TMA has read them the drain signals stage_free, which
-// the compute warpgroups wait for before writing the next tile's dS.
+// d = 64: the dQ product keeps queries as lanes (dQ^T would have only 64 lanes), and
+// the accumulator holds each head as [16][rows][4], so that a lane's four consecutive
+// head-dim entries are one 16-byte reduction and a warp's 32 rows 512 contiguous bytes.
+// (Staging dQ through the freed dS tile and adding it with TMA reduce-adds instead made
+// the compute warpgroups wait for the tile: padded workload's backward 0.638 ms, against
+// 0.549 with these reductions.)
 // kGrouped: CTAs ordered heaviest first across groups of heads (a separate instantiation:
 // the mapping costs the d = 128 kernel a few spilled registers, so launches that keep one
 // head at a time use the plain one).
@@ -312,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     mbar_init(&sm.dp_full, 1);
     mbar_init(&sm.ds_empty, 1);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.stage_free, kKeys);
     mbar_init(&sm.dq_empty, kKeys);
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.drain, 1);
@@ -340,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tma_prefetch_desc(&p.tk);
     tma_prefetch_desc(&p.tv);
     tma_prefetch_desc(&p.tdo);
-    tma_prefetch_desc(&p.tdq);
     mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
     const TmaRow rk = tma_row(p.ak, b, kv0, h);
     for (int c = 0; c < kChunks; ++c) {
@@ -451,14 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mma_commit(&sm.dq_full);
         issue_dk();
       } else {
-        // dQ = dS K: A = dS (queries contiguous), B = K (head-dim contiguous).  The
-        // warpgroups stage dQ in the dS tile, so dq_full waits for dK's last read of it.
-        issue_dk();
+        // dQ = dS K: A = dS (queries contiguous), B = K (head-dim contiguous).  Issued
+        // before dK so that its read-out and reductions overlap the dK products.
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           mma_ss(tmem + kColDQ, sdesc_sw128(ds_addr + kk * 2048, 16384, 1024),
                  sdesc_sw128(k_addr + kk * 2048, 16384, 1024), kIdQ, kk > 0);
         mma_commit(&sm.dq_full);
+        issue_dk();
       }
       // the dS tile and Q_i have no reader left
       mma_commit(&sm.ds_empty);
@@ -552,10 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
       // dS = P (dP - D) once dP^T is in TMEM and the MMAs of the previous tile have
       // finished reading the dS tile
       ok = mbar_wait(&sm.dp_full, it & 1, p.status, abort_flag);
-      // (d = 64: and the drain has staged and sent the previous tile's dQ from it)
       if (it > 0)
-        ok = ok && mbar_wait(D == 128 ? &sm.ds_empty : &sm.stage_free, (it - 1) & 1, p.status,
-                             abort_flag);
+        ok = ok && mbar_wait(&sm.ds_empty, (it - 1) & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -670,40 +693,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             if ((i % 2) == 1) __nanosleep(kDrainPaceNs);
           }
       } else {
-        // dQ: lane = query row q0 + quad * 32 + lane, columns = the 64 head-dim entries
+        // dQ: lane = query row q0 + quad * 32 + lane, columns = the 64 head-dim entries.
+        // The accumulator holds each head as [d / 4][rows][4]: a lane's four consecutive
+        // head-dim entries are 16 bytes, and the warp's 32 rows 512 contiguous bytes.
         uint32_t r[2][32];
         tmem_ld32(lane_base + kColDQ, r[0]);
         tmem_ld32(lane_base + kColDQ + 32, r[1]);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
-        // stage the warp's 32 rows as two 32 x 32 boxes (128-byte swizzle) in its two
-        // slices of the dS tile, which the completed dK and dQ products no longer read,
-        // reduce them into the accumulator with TMA, and hand the tile back once TMA has
-        // read them
+        float* dst = p.dq_acc + static_cast<int64_t>(bh) * p.rows * D +
+                     (static_cast<int64_t>(q0) + quad * 32 + lane) * 4;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint8_t* srow = sm.ds + c * 16384 + quad * 4096 + lane * 128;
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(srow + ((u ^ (lane & 7)) * 16)) =
-                make_uint4(r[c][4 * u], r[c][4 * u + 1], r[c][4 * u + 2], r[c][4 * u + 3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int row = static_cast<int>(static_cast<int64_t>(bh) * p.rows) + q0 + quad * 32;
-          tma_reduce_add_2d(&p.tdq, sm.ds + quad * 4096, 0, row);
-          tma_reduce_add_2d(&p.tdq, sm.ds + 16384 + quad * 4096, 32, row);
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-        __syncwarp();
-        mbar_arrive(&sm.stage_free);
+          for (int j = 0; j < 8; ++j) {
+            red_add_v4(dst + static_cast<int64_t>(c * 8 + j) * p.rows * 4,
+                       __uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
+                       __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3]));
+            __nanosleep(2 * kDrainPaceNs);
+          }
       }
     }
-    // the accumulator adds must be complete before the CTA exits
-    if (lane == 0) bulk_wait_all();
+    // the drain warps meet here before the common exit (without this reconvergence
+    // point ptxas spills registers in every instantiation of the kernel)
     __syncwarp();
   }
   tc_fence_before();
@@ -761,7 +774,6 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     p.tk = a.tk;
     p.tv = a.tv;
     p.tdo = a.tdo;
-    p.tdq = a.tdq;
     p.stats = a.row_stats;
     p.dq_acc = a.dq_acc;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
@@ -812,7 +824,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
         bwd_dq_convert_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
             a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.aq, g.B, g.H, g.sq, rows, g.scale);
       else
-        bwd_dq_convert_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        bwd_dq_convert_d4_kernel<<<static_cast<unsigned>((bh * g.sq + 255) / 256), 256, 0,
+                                   stream>>>(
             a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.aq, g.B, g.H, g.sq, rows, g.scale);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -127,9 +127,6 @@ RowAddr shard_rows(int N, int b, int S, int H, int d);
 bool encode_rows_map(CUtensorMap* map, const void* base, int d, int heads_total, int shards,
                      const RowAddr& a);
 
-// 2-D TMA map over the fp32 dQ accumulator viewed as [rows_total][d], box = 32
-// columns x 32 rows, 128-byte swizzle (the backward reduces dQ tiles into it).
-bool encode_acc_map(CUtensorMap* map, const float* base, int d, int64_t rows_total);
 
 // 2-D TMA map over a bf16 matrix of `outer` rows of `inner` elements at a pitch of
 // `pitch` elements, box = box_inner x box_outer, 128-byte swizzle (box_inner = 64).
@@ -165,7 +162,6 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo;
-  CUtensorMap tdq;     // over dq_acc (encode_acc_map)
   RowAddr aq, ak, av, ao;   // layouts of q/dq, k/dk, v/dv, o/dout
   const void* o;
   const void* dout;
@@ -173,7 +169,7 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;      // workspace: [B][H][rows][d] fp32
+  float* dq_acc;      // workspace: fp32, [B][H] blocks of rows * d (layout per d in attn_bwd.cu)
   float* row_stats;   // workspace: [B][H][2][rows] fp32 (-lse*log2e, D)
   bool dq_accumulate; // keep dq_acc from the previous call instead of zeroing it
   AttnGeom g;

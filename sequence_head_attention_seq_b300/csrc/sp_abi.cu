@@ -250,19 +250,6 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int d, int heads_total,
   return r == CUDA_SUCCESS;
 }
 
-bool encode_acc_map(CUtensorMap* map, const float* base, int d, int64_t rows_total) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows_total)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t elem[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
-                        strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 // Row layouts of the attention tensors: plain strided [B][S][H][d], or all eight in the
 // sequence-shard layout [N][B/N][S/N][N*H][d].
@@ -470,10 +457,6 @@ sp_status sp_attn_bwd(const sp_attn_params* p, const void* o, const float* lse, 
   a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.dq_off);
   a.row_stats = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.stats_off);
   a.dq_accumulate = p->dq_accumulate != 0;
-  if (g.sq > 0 && g.sk > 0 &&
-      !encode_acc_map(&a.tdq, a.dq_acc, g.d,
-                      static_cast<int64_t>(g.B) * g.H * padded_rows(g.sq)))
-    return SP_ERR_CUDA;
   a.g = g;
   a.status = status_word();
   if (a.status == nullptr) return SP_ERR_CUDA;
