@@ -291,7 +291,25 @@ def cpu_baseline(w, ins, head=0):
     line["single_core"] = {"value": f1 / dt1 / 1e12, "unit": UNIT, "cores": 1,
                            "sample": f"1 head over the first {p1} positions; "
                                      f"{f1 / 1e9:.1f} GFLOP in {dt1:.1f} s"}
+    line["relayout"] = cpu_relayout(w, ins)
     return line
+
+
+def cpu_relayout(w, ins):
+    """The regrouping on the host: the oracle's scalar copy loop (one thread) over one
+    whole tensor of the workload (Q, sequence shards -> head groups), in GB/s of bytes
+    read + written; None when the workload has a single shard (nothing to regroup)."""
+    if w.N == 1:
+        return None
+    import oracle
+    bits = ins["q"].contiguous().cpu().view(torch.int16).numpy().view("uint16")
+    t0 = time.perf_counter()
+    oracle.default().seq2head(bits, w.N, w.b, w.s, w.h, w.d)
+    dt = time.perf_counter() - t0
+    return {"value": 2 * bits.nbytes / dt / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"seq2head of one {bits.nbytes / 2**20:.0f} MiB tensor (Q) of {w.name}, "
+                      f"N={w.N}: {dt:.2f} s"}
 
 
 # ---------------------------------------------------------------- arms

@@ -55,3 +55,15 @@ def test_reference_arm_prints_the_contract_line():
     assert "first 128 positions" in cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_cpu_relayout_rate_on_a_small_workload():
+    """The host regrouping rate in `cpu_baseline` (the oracle's copy loop over one tensor)
+    runs on CPU tensors and reports bytes read + written per second."""
+    w = workloads.Workload("t", 3, b=2, h=4, d=64, s=256, N=2, causal=True, scale=1.0)
+    ins = workloads.make_inputs(w, device="cpu", with_dout=False)
+    r = bench.cpu_relayout(w, ins)
+    assert r["unit"] == "GB/s" and r["value"] > 0 and r["cores"] == 1
+    assert "seq2head" in r["sample"]
+    one = workloads.Workload("t1", 4, b=1, h=2, d=64, s=128, N=1, causal=True, scale=1.0)
+    assert bench.cpu_relayout(one, workloads.make_inputs(one, with_dout=False)) is None
