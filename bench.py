@@ -487,6 +487,33 @@ def measure_workload(w, steps, warmup, device, peaks):
     return out
 
 
+# a workload whose whole fwd+bwd the oracle finishes in about half a minute or less on the
+# host cores (about 0.04 TFLOP/s on 16) is timed in full beside its GPU line
+ORACLE_WHOLE_MAX_FLOPS = 1.0e12
+
+
+def oracle_whole(w, ins):
+    """The oracle on the host cores over the whole workload: every head, query row and key
+    of forward and backward (the regroupings are not part of it)."""
+    import oracle
+    orc = oracle.default()
+
+    def plain(t):   # shards [N][b][s/N][h][d] -> [b][s][h][d] (the shards in order)
+        return t.permute(1, 0, 2, 3, 4).reshape(w.b, w.s, w.h, w.d).double().cpu().numpy()
+
+    q, k, v, do = (plain(ins[n]) for n in ("q", "k", "v", "dout"))
+    kl = None if ins["key_len"] is None else ins["key_len"].tolist()
+    t0 = time.perf_counter()
+    orc.attn_fwd(q, k, v, w.causal, 0, kl)
+    orc.attn_bwd(q, k, v, do, w.causal, 0, kl)
+    dt = time.perf_counter() - t0
+    return {"value": step_flops(w) / dt / 1e12, "unit": UNIT, "cores": orc.threads(),
+            "kind": "oracle",
+            "sample": f"fp64 C oracle, fwd+bwd of the whole {w.name} workload (all {w.b * w.h} "
+                      f"heads, every row and key; inputs of the same shapes and distributions "
+                      f"generated on the host): {step_flops(w) / 1e9:.1f} GFLOP in {dt:.1f} s"}
+
+
 def measure_other_workloads(warmup, device, peaks, local):
     clocks = ClockSampler(gpu_index_for(local))
     clocks.start()
@@ -498,6 +525,11 @@ def measure_other_workloads(warmup, device, peaks, local):
     finally:
         clocks.stop()
     res["clocks"] = clocks.summary()
+    # the oracle after the GPU timing, so that the clock record covers the kernels only
+    for name, _ in OTHER_WORKLOADS:
+        w = workloads.WORKLOADS[name]
+        if step_flops(w) <= ORACLE_WHOLE_MAX_FLOPS:
+            res[name]["cpu_baseline"] = oracle_whole(w, workloads.make_inputs(w, device="cpu"))
     res["peaks"] = "burst bf16 and HBM copy from " + ("MEASURED_PEAKS.json" if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else "the fallback figures")
     return res

@@ -67,3 +67,13 @@ def test_cpu_relayout_rate_on_a_small_workload():
     assert "seq2head" in r["sample"]
     one = workloads.Workload("t1", 4, b=1, h=2, d=64, s=128, N=1, causal=True, scale=1.0)
     assert bench.cpu_relayout(one, workloads.make_inputs(one, with_dout=False)) is None
+
+
+def test_oracle_whole_on_a_small_workload():
+    """The whole-workload oracle timing that the small workloads' entries carry: the
+    shards are put back in sequence order and every head, row and key is computed."""
+    w = workloads.Workload("t", 5, b=2, h=2, d=64, s=128, N=2, causal=False, scale=1.0,
+                           key_len_range=(64, 128))
+    r = bench.oracle_whole(w, workloads.make_inputs(w, device="cpu"))
+    assert r["kind"] == "oracle" and r["value"] > 0 and r["cores"] >= 1
+    assert "all 4 heads" in r["sample"]
