@@ -326,7 +326,7 @@ sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o, const floa
  * s/N rows of (h/N)*d elements at a pitch of h*d; one copy when b = 1) between the host
  * shard layout and a head-major device buffer, and back for the results.  Group g's
  * copies in, its forward and backward on `stream`, and its copies out run on three
- * streams with group g+1's transfers overlapping group g's kernels (two buffer slots);
+ * streams with group g+1's transfers overlapping group g's kernels (three buffer slots);
  * the first and the last group go as two halves of their heads, which halves the
  * transfers that no kernel can hide.
  *
@@ -341,7 +341,7 @@ sp_status sp_attn_bwd_noalloc(const sp_attn_params* p, const void* o, const floa
  * key_len         : NULL or DEVICE int32 [b] (keys of batch row bb: j < key_len[bb]).
  * softmax_scale   : <= 0 selects 1/sqrt(d).
  * workspace       : DEVICE, >= sp_ulysses_host_workspace_size(...) bytes, 256-byte
- *                   aligned, owned by the caller (two slots of eight group tensors, the
+ *                   aligned, owned by the caller (three slots of eight group tensors, the
  *                   lse, and the backward workspace).
  * stream          : the kernels run on it, and it waits for the last result to reach
  *                   the host.  h2d_stream, d2h_stream: two further streams, distinct from

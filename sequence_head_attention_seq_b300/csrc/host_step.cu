@@ -8,16 +8,20 @@
 // copy engines move each head group between the host shard layout and a head-major
 // device buffer while they transfer it, and no relayout kernel runs on this path.
 //
-// Per head group g (slot = g % 2, two slots so that group g+1 moves while g computes):
-//   h2d stream     : Q, K, V of g into the slot            -> qkv_ready[slot]
-//                    dO of g                               -> do_ready[slot]
-//   compute stream : attention forward of g (waits qkv_ready, and out_free of g-2)
+// Per unit u, a head group or half of one (slot = u % 3: unit u+1's inputs move in and
+// unit u-1's results move out while u computes, and the third slot lets the inputs run
+// a whole unit ahead):
+//   h2d stream     : Q, K, V of u into the slot            -> qkv_ready[slot]
+//                    dO of u                               -> do_ready[slot]
+//   compute stream : attention forward of u (waits qkv_ready, and out_free of u-3)
 //                                                          -> o_ready[slot]
-//                    attention backward of g (waits do_ready) -> grads_ready[slot]
-//   d2h stream     : O of g to the host (waits o_ready), then dQ, dK, dV (waits
+//                    attention backward of u (waits do_ready) -> grads_ready[slot]
+//   d2h stream     : O of u to the host (waits o_ready), then dQ, dK, dV (waits
 //                    grads_ready)                          -> out_free[slot]
 // The h2d stream refills a slot only after the backward that last read it
-// (grads_ready of g-2).  The first and the last head group go as two halves of their
+// (grads_ready of u-3).  (Measured on B300, 70B-shaped step from host memory: two slots
+// 61.44-61.75 ms, three 60.97-61.40 ms: with the host link about as fast as the kernels,
+// the inputs of the next unit no longer wait for the backward two units back.)  The first and the last head group go as two halves of their
 // heads: only the first unit's inputs and the last unit's results are not overlapped
 // with kernels, so halving those units halves the exposed transfer time.  Events are created for the call and released at its end
 // (their pending records complete on their own); no device memory is allocated.
@@ -31,6 +35,7 @@ namespace sp {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kSlots = 3;   // device buffer slots the units cycle through
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -93,7 +98,7 @@ Layout layout_of(const HostGeom& g, int causal) {
   const sp_attn_params p = group_params(g, g.H, stand_in, stand_in, stand_in, causal, nullptr,
                                        0.0f);
   l.bwd = align_up(sp_attn_bwd_workspace_size(&p));
-  l.total = 2 * l.slot + l.bwd;
+  l.total = kSlots * l.slot + l.bwd;
   return l;
 }
 
@@ -138,7 +143,7 @@ bool pinned_host(const void* p) {
 }
 
 struct Events {
-  static constexpr int kCount = 12;
+  static constexpr int kCount = 2 + 5 * kSlots;
   cudaEvent_t e[kCount] = {};
   bool create() {
     for (auto& x : e)
@@ -199,14 +204,21 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
   cudaStream_t ds = static_cast<cudaStream_t>(d2h_stream);
   Events ev;
   if (!ev.create()) return SP_ERR_CUDA;
-  cudaEvent_t start = ev.e[0], qkv_ready[2] = {ev.e[1], ev.e[2]}, do_ready[2] = {ev.e[3], ev.e[4]},
-              o_ready[2] = {ev.e[5], ev.e[6]}, grads_ready[2] = {ev.e[7], ev.e[8]},
-              out_free[2] = {ev.e[9], ev.e[10]}, done = ev.e[11];
+  cudaEvent_t start = ev.e[0], done = ev.e[1];
+  cudaEvent_t qkv_ready[kSlots], do_ready[kSlots], o_ready[kSlots], grads_ready[kSlots],
+      out_free[kSlots];
+  for (int i = 0; i < kSlots; ++i) {
+    qkv_ready[i] = ev.e[2 + i];
+    do_ready[i] = ev.e[2 + kSlots + i];
+    o_ready[i] = ev.e[2 + 2 * kSlots + i];
+    grads_ready[i] = ev.e[2 + 3 * kSlots + i];
+    out_free[i] = ev.e[2 + 4 * kSlots + i];
+  }
 
   char* ws = static_cast<char*>(workspace);
   auto slot_tensor = [&](int slot, int t) { return ws + slot * lay.slot + t * lay.tensor; };
   auto slot_lse = [&](int slot) { return reinterpret_cast<float*>(ws + slot * lay.slot + 8 * lay.tensor); };
-  void* bwd_ws = ws + 2 * lay.slot;
+  void* bwd_ws = ws + kSlots * lay.slot;
 
 #define SP_CHECK(x)                            \
   do {                                         \
@@ -235,9 +247,9 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
   auto enqueue_units = [&]() -> sp_status {
     for (size_t ui = 0; ui < units.size(); ++ui) {
       const Unit& u = units[ui];
-      const int slot = static_cast<int>(ui & 1);
+      const int slot = static_cast<int>(ui % kSlots);
       // slot tensors: 0 q, 1 k, 2 v, 3 dout, 4 o, 5 dq, 6 dk, 7 dv
-      if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(hs, grads_ready[slot], 0));
+      if (ui >= kSlots) SP_CHECK(cudaStreamWaitEvent(hs, grads_ready[slot], 0));
       for (int t = 0; t < 3; ++t)
         SP_CHECK(copy_unit(g, u, const_cast<void*>(in[t]), slot_tensor(slot, t), true, hs));
       SP_CHECK(cudaEventRecord(qkv_ready[slot], hs));
@@ -245,7 +257,7 @@ sp_status sp_ulysses_step_host(const sp_ulysses_host_params* p, void* workspace,
       SP_CHECK(cudaEventRecord(do_ready[slot], hs));
 
       SP_CHECK(cudaStreamWaitEvent(cs, qkv_ready[slot], 0));
-      if (ui >= 2) SP_CHECK(cudaStreamWaitEvent(cs, out_free[slot], 0));
+      if (ui >= kSlots) SP_CHECK(cudaStreamWaitEvent(cs, out_free[slot], 0));
       const sp_attn_params ap = group_params(g, u.nh, slot_tensor(slot, 0), slot_tensor(slot, 1),
                                              slot_tensor(slot, 2), p->causal, p->key_len,
                                              p->softmax_scale);
