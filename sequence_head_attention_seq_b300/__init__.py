@@ -13,6 +13,8 @@ The computation lives in ``libsp.so`` (C ABI in ``include/sp.h``, CUDA kernels i
     UlyssesHostStep / sp_ulysses_step_host        the step on host shards, transfers overlapped
     ring_attention_fwd / ring_attention_bwd       blockwise attention over key chunks
     AttentionLayer                                projections + regrouping + attention
+    attention / seq_all_to_all / ulysses_attention  the same calls as torch.autograd
+                                                  Functions (gradients through libsp)
 
 Nothing here computes attention in Python; if the native library is missing the
 calls raise.
@@ -23,6 +25,7 @@ from .binding import (SpError, sp_attn_bwd, sp_attn_bwd_workspace_size, sp_attn_
                       sp_relayout_head2seq_packed, sp_relayout_seq2head,
                       sp_relayout_seq2head_packed, sp_status_string,
                       sp_ulysses_host_workspace_size, sp_ulysses_step_host)
+from .autograd import attention, seq_all_to_all, ulysses_attention
 from .pipeline import (AttentionLayer, UlyssesAttention, UlyssesHostStep, ring_attention_bwd,
                        ring_attention_fwd)
 
@@ -32,4 +35,4 @@ __all__ = ["SpError", "sp_attn_bwd", "sp_attn_bwd_workspace_size", "sp_attn_fwd"
            "sp_linear_bwd",
            "sp_status_string", "sp_ulysses_host_workspace_size", "sp_ulysses_step_host",
            "UlyssesAttention", "UlyssesHostStep", "AttentionLayer", "ring_attention_fwd",
-           "ring_attention_bwd"]
+           "ring_attention_bwd", "attention", "seq_all_to_all", "ulysses_attention"]
