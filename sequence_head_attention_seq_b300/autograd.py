@@ -7,7 +7,8 @@ long-context-attention issue wraps an all-to-all (sequence shards -> head groups
 local attention and the inverse all-to-all, and its backward runs the same three steps in
 reverse (the all-to-all of the gradients goes the other way).  Every step runs in libsp;
 these Functions only route tensors and keep what the backward needs (q, k, v, out and the
-per-row log-sum-exp).
+per-row log-sum-exp).  The backward passes are not themselves differentiable (no
+second-order gradients).
 
     attention(q, k, v, ...)            softmax(q k^T * scale + mask) v, [B][s][H][d] tensors
                                        or [N][b][s/N][N*H][d] sequence shards
@@ -19,6 +20,7 @@ per-row log-sum-exp).
 from __future__ import annotations
 
 import torch
+from torch.autograd.function import once_differentiable
 
 from .binding import (sp_attn_bwd, sp_attn_fwd, sp_relayout, sp_relayout_head2seq,
                       sp_relayout_seq2head)
@@ -36,6 +38,7 @@ class _Attention(torch.autograd.Function):
         return o
 
     @staticmethod
+    @once_differentiable
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
         causal, q_offset, key_len, softmax_scale, key_mask = ctx.args
@@ -69,6 +72,7 @@ class _SeqAllToAll(torch.autograd.Function):
         return sp_relayout(x.contiguous(), N, scatter_dim, gather_dim)
 
     @staticmethod
+    @once_differentiable
     def backward(ctx, g):
         N, scatter_dim, gather_dim = ctx.args
         return sp_relayout(g.contiguous(), N, gather_dim, scatter_dim), None, None, None
@@ -101,6 +105,7 @@ class _ShardsToGroups(torch.autograd.Function):
         return tuple(outs)
 
     @staticmethod
+    @once_differentiable
     def backward(ctx, *grads):
         return (None, *sp_relayout_head2seq(_full_grads(grads, ctx.shapes), ctx.N))
 
@@ -116,6 +121,7 @@ class _GroupsToShards(torch.autograd.Function):
         return tuple(outs)
 
     @staticmethod
+    @once_differentiable
     def backward(ctx, *grads):
         return (None, *sp_relayout_seq2head(_full_grads(grads, ctx.shapes), ctx.N))
 
