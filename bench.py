@@ -491,7 +491,9 @@ def measure_workload(w, steps, warmup, device, peaks, graph: bool = False):
         step.forward(ins["q"], ins["k"], ins["v"])
         step.backward(ins["dout"])
     torch.cuda.synchronize()
-    timer.enabled = True
+    # the step rate from a loop without per-call events (on sub-millisecond steps the
+    # twelve event records per step would show), then the per-call times from a second,
+    # instrumented loop of the same steps
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(steps):
@@ -499,10 +501,15 @@ def measure_workload(w, steps, warmup, device, peaks, graph: bool = False):
         step.backward(ins["dout"])
     b.record()
     torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    timer.enabled = True
+    for _ in range(steps):
+        step.forward(ins["q"], ins["k"], ins["v"])
+        step.backward(ins["dout"])
+    torch.cuda.synchronize()
     timer.enabled = False
     if sp_get_device_status() != 0:
         raise RuntimeError(f"device status reported an error in workload {w.name}")
-    ms = a.elapsed_time(b) / steps
     per_step = timer.per_step_ms(steps)
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
