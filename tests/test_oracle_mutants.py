@@ -69,3 +69,36 @@ def test_mutant_is_caught(name, tmp_path):
         except (AssertionError, ValueError):
             caught.append(pin.__name__)
     assert caught, f"mutant {name} passed every pin"
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_fails_a_generated_property(name, tmp_path):
+    """The same mutants against the generated properties of test_oracle_properties.py:
+    hypothesis searches (without shrinking) for a case on which the broken oracle
+    disagrees with torch's fp64 attention, the split-key merge identity or torch's
+    regrouping."""
+    from hypothesis import Phase, find, settings
+    from hypothesis.errors import NoSuchExample
+    from test_oracle_properties import PROPERTIES
+    old, new = MUTANTS[name]
+    mutated = tmp_path / "oracle_mutant.c"
+    mutated.write_text(open(SRC).read().replace(old, new, 1))
+    orc = oracle.Oracle(oracle.open_library(
+        oracle.compile_source(str(mutated), str(tmp_path / "m.so"))))
+    search = settings(max_examples=60, phases=[Phase.generate], derandomize=True,
+                      database=None, deadline=None)
+
+    def fails(check, case):
+        try:
+            check(orc, case)
+        except (AssertionError, ValueError):
+            return True
+        return False
+
+    for strategy, check in PROPERTIES:
+        try:
+            find(strategy, lambda case, check=check: fails(check, case), settings=search)
+            return
+        except NoSuchExample:
+            continue
+    pytest.fail(f"mutant {name} passed every generated property")
