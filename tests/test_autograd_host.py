@@ -133,3 +133,29 @@ def test_seq_all_to_all_gradient_goes_the_other_way(rec):
                          ("sp_relayout", {"N": N, "shape": (b, s, h // N, d), "scatter": 1,
                                           "gather": 2})]
     assert x.grad.shape == x.shape
+
+
+# ---------------------------------------------------------------- the step class itself
+
+def test_ulysses_step_calls(rec):
+    """UlyssesAttention (the benchmark's step): the same six library calls per step,
+    buffers reused from one step to the next."""
+    from sequence_head_attention_seq_b300 import UlyssesAttention
+    N, b, s, h, d = 2, 1, 256, 4, 128
+    step = UlyssesAttention(N, b, s, h, d, causal=True, device="cpu")
+    rec.calls.clear()
+    shards = [torch.zeros((N, b, s // N, h, d), dtype=torch.bfloat16) for _ in range(4)]
+    outs = []
+    for _ in range(2):
+        o = step.forward(*shards[:3])
+        grads = step.backward(shards[3])
+        outs.append((o.data_ptr(),) + tuple(g.data_ptr() for g in grads))
+    names = [c[0] for c in rec.calls]
+    one = ["sp_relayout_seq2head", "sp_attn_fwd", "sp_relayout_head2seq",
+           "sp_relayout_seq2head", "sp_attn_bwd_workspace_size", "sp_attn_bwd",
+           "sp_relayout_head2seq"]
+    assert names == one + one
+    assert outs[0] == outs[1]                  # the same output buffers every step
+    group = {"B": N * b, "H": h // N, "sq": s, "sk": s, "d": d, "causal": 1, "shards": 1}
+    assert rec.calls[1][1] == group and rec.calls[5][1] == group
+
